@@ -1,0 +1,151 @@
+/* TEST INFRASTRUCTURE ONLY.  A plain, slow fp64 CPU oracle for the
+ * multi-head attention forward pass.  Only the tests, the smoke check and
+ * the CPU-baseline leg of the benchmark load this file; the library's
+ * product path never does, and the two share no code.
+ *
+ * What it computes is the definition of attention, written out directly:
+ *
+ *   "Simple FlashAttention" (Triton-learning blog, Puzzle 9, problem
+ *   statement): z_i = sum_j softmax(q_i k_1, ..., q_i k_T)_j v_j.
+ *   Numerically safe softmax subtracts the row maximum first (same blog,
+ *   Puzzle 8 problem statement).  FlashAttention-2 (ML-Triton paper,
+ *   section 2.5, Algorithm 1) reaches exactly this result tile by tile.
+ *
+ * Readings of points the pages leave open (all fixed by the library's
+ * interface, not by the pages):
+ *   - scores are scaled: s_ij = scale * <q_i, k_j>, scale used as passed;
+ *   - causal means square, top-left aligned: row i sees keys 0..i;
+ *   - LSE_i = m_i + ln(l_i) in natural log on the scaled scores;
+ *   - a row with an empty key set (never produced by a square mask) gets
+ *     O = 0 and LSE = -inf.
+ *
+ * Inputs are bfloat16 bit patterns; each is widened exactly to double.
+ * All arithmetic is fp64: the dot product in index order, then the row
+ * maximum m, l = sum exp(s - m), P = exp(s - m) / l, O = sum_j P_j v_j.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static double bf16_to_f64(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+/* One query row i of one head.  q_bh, k_bh, v_bh: [N, d] bf16 bits.
+ * s: scratch of N doubles.  o_row: d doubles out.  p_row: optional N
+ * doubles out (the softmax probabilities; zero for keys outside J_i). */
+static void attention_row(const uint16_t *q_bh, const uint16_t *k_bh, const uint16_t *v_bh,
+                          int64_t N, int64_t d, double scale, int causal, int64_t i,
+                          double *s, double *o_row, double *lse, double *p_row) {
+    /* key set J_i = {0..N-1}, or {0..i} under the causal mask */
+    int64_t nk = causal ? i + 1 : N;
+    if (nk > N) nk = N;
+    for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
+    if (p_row)
+        for (int64_t j = 0; j < N; ++j) p_row[j] = 0.0;
+    if (nk <= 0) {
+        *lse = -INFINITY;
+        return;
+    }
+    /* scores s_ij = scale * sum_c q_ic k_jc */
+    for (int64_t j = 0; j < nk; ++j) {
+        double acc = 0.0;
+        for (int64_t c = 0; c < d; ++c)
+            acc += bf16_to_f64(q_bh[i * d + c]) * bf16_to_f64(k_bh[j * d + c]);
+        s[j] = scale * acc;
+    }
+    /* row maximum and the sum of shifted exponentials */
+    double m = s[0];
+    for (int64_t j = 1; j < nk; ++j)
+        if (s[j] > m) m = s[j];
+    double l = 0.0;
+    for (int64_t j = 0; j < nk; ++j) l += exp(s[j] - m);
+    /* O_i = sum_j P_ij v_j with P_ij = exp(s_ij - m_i) / l_i */
+    for (int64_t j = 0; j < nk; ++j) {
+        double p = exp(s[j] - m) / l;
+        if (p_row) p_row[j] = p;
+        for (int64_t c = 0; c < d; ++c) o_row[c] += p * bf16_to_f64(v_bh[j * d + c]);
+    }
+    *lse = m + log(l);
+}
+
+/* Rows rows[0..nrows-1] of one head.  o_out: [nrows, d]; lse_out: [nrows].
+ * nthreads <= 0 uses the OpenMP default.  Returns 0, or -1 on bad input. */
+int oracle_attention_rows(const uint16_t *q_bh, const uint16_t *k_bh, const uint16_t *v_bh,
+                          int64_t N, int64_t d, float scale, int causal,
+                          const int64_t *rows, int64_t nrows,
+                          double *o_out, double *lse_out, int nthreads) {
+    if (N < 0 || d <= 0 || nrows < 0) return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return -1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#else
+    nthreads = 1;
+#endif
+    int bad = 0;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+        if (!s) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 4)
+            for (int64_t r = 0; r < nrows; ++r)
+                attention_row(q_bh, k_bh, v_bh, N, d, (double)scale, causal, rows[r], s,
+                              o_out + r * d, lse_out + r, NULL);
+            free(s);
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+/* Every row of every head: q, k, v are [BH, N, d]; o_out [BH, N, d];
+ * lse_out [BH, N]. */
+int oracle_attention_fwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         int64_t BH, int64_t N, int64_t d, float scale, int causal,
+                         double *o_out, double *lse_out, int nthreads) {
+    if (BH < 0 || N < 0 || d <= 0) return -1;
+    int64_t *rows = (int64_t *)malloc(sizeof(int64_t) * (size_t)(N > 0 ? N : 1));
+    if (!rows) return -1;
+    for (int64_t i = 0; i < N; ++i) rows[i] = i;
+    int rc = 0;
+    for (int64_t bh = 0; bh < BH && rc == 0; ++bh) {
+        const int64_t off = bh * N * d;
+        rc = oracle_attention_rows(q + off, k + off, v + off, N, d, scale, causal, rows, N,
+                                   o_out + off, lse_out + bh * N, nthreads);
+    }
+    free(rows);
+    return rc;
+}
+
+/* The probability matrix P [N, N] of one head (zeros outside each row's
+ * key set) together with LSE [N]; for checks of the softmax itself. */
+int oracle_attention_probs(const uint16_t *q_bh, const uint16_t *k_bh, const uint16_t *v_bh,
+                           int64_t N, int64_t d, float scale, int causal,
+                           double *p_out, double *o_out, double *lse_out) {
+    if (N < 0 || d <= 0) return -1;
+    double *s = (double *)malloc(sizeof(double) * (size_t)(N > 0 ? N : 1));
+    if (!s) return -1;
+    for (int64_t i = 0; i < N; ++i)
+        attention_row(q_bh, k_bh, v_bh, N, d, (double)scale, causal, i, s, o_out + i * d,
+                      lse_out + i, p_out + i * N);
+    free(s);
+    return 0;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

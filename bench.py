@@ -1,0 +1,371 @@
+"""Benchmark of the fused attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+                    [--impl ours|reference] [--no-cpu-baseline]
+
+One step is one attention forward pass (the whole hot path: Q/K/V tile
+loads, S = Q K^T, masked online softmax, O += P V, O/LSE epilogue) over one
+synthetic batch.  The default workload is the long-sequence causal case
+B=1, H=32, N=16384, d=128 ("cfg5"); other names are listed in synth.CONFIGS.
+
+Metric: attention forward TFLOP/s, counting 4*B*H*N^2*d FLOPs per pass
+(half of that with the causal mask), aggregated over all ranks.  Rank 0
+prints one JSON line.  Under torchrun each rank runs its own independent
+batch (a replica with its own seed; weak scaling, no data-path collective).
+
+`--impl reference` times the fp64 CPU oracle (the reference arm) on a
+bounded sample of rows of the same workload, on this machine's host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "attention fwd TFLOP/s and % of GB300 bf16 tensor peak, per (B,H,N,d,causal)"
+UNIT = "TFLOP/s"
+FALLBACK_PEAK_TFLOPS = 1900.0  # used only when MEASURED_PEAKS.json is absent
+
+
+def counted_flops(c) -> float:
+    f = 4.0 * c["B"] * c["H"] * c["N"] * c["N"] * c["d"]
+    return f / 2 if c["causal"] else f
+
+
+def workload_name(name, c) -> str:
+    return (f"{name}: B={c['B']},H={c['H']},N={c['N']},d={c['d']},"
+            f"{'causal' if c['causal'] else 'non-causal'}")
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    return FALLBACK_PEAK_TFLOPS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def kernel_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "head_attention_forward_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; otherwise None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    ent = rec.get(name)
+    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample(c, q, k, v, rows_per_head: int, heads, nthreads: int = 0):
+    """Times the oracle on `rows_per_head` evenly spread rows of each head in
+    `heads`; returns (seconds, counted FLOPs of those rows, rows)."""
+    import oracle
+    N, d = c["N"], c["d"]
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    rows = np.unique(np.linspace(0, N - 1, rows_per_head).astype(np.int64))
+    per_row = 4.0 * N * d * (0.5 if c["causal"] else 1.0)
+    t0 = time.perf_counter()
+    for bh in heads:
+        oracle.attention_rows(q, k, v, scale, c["causal"], int(bh), rows, nthreads)
+    dt = time.perf_counter() - t0
+    return dt, per_row * rows.size * len(heads), rows.size * len(heads)
+
+
+def size_oracle_sample(c, q, k, v, target_s: float):
+    """Rows per head for one head so that the oracle runs about target_s."""
+    import oracle
+    oracle.build()
+    dt, _, n = oracle_sample(c, q, k, v, 16, [0])
+    per_row = max(dt / max(n, 1), 1e-6)
+    return int(min(c["N"], max(16, target_s / per_row)))
+
+
+def run_reference(args, c, name):
+    """Reference arm: the fp64 oracle on the host cores, per step a bounded
+    sample of rows of the same workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import oracle
+    q, k, v = synth.qkv(c["seed"], c["B"], c["H"], c["N"], c["d"], c["sigma_qk"], c["sigma_v"])
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    rows = size_oracle_sample(c, q, k, v, budget)
+    for i in range(args.warmup):
+        oracle_sample(c, q, k, v, rows, [i % (c["B"] * c["H"])])
+    tot_t, tot_f, tot_rows = 0.0, 0.0, 0
+    for i in range(args.steps):
+        dt, fl, nr = oracle_sample(c, q, k, v, rows, [(i + args.warmup) % (c["B"] * c["H"])])
+        tot_t += dt
+        tot_f += fl
+        tot_rows += nr
+    value = tot_f / tot_t / 1e12
+    cores = oracle.num_threads()
+    sample = f"{rows} evenly spaced query rows of one head per step ({tot_rows} rows total)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": workload_name(name, c)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="cfg5", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    name = args.config
+    c = synth.CONFIGS[name]
+    if args.impl == "reference":
+        return run_reference(args, c, name)
+    if args.warmup < 3:
+        print("note: fewer than 3 warm-up steps; the number is not a bench value", file=sys.stderr)
+
+    import torch
+
+    import head_attention_forward_gb300 as mha
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    mha.build()
+    mha.lib()
+
+    B, H, N, d, causal = c["B"], c["H"], c["N"], c["d"], c["causal"]
+    seed = c["seed"] + 1000 * rank
+    qb, kb, vb = synth.qkv(seed, B, H, N, d, c["sigma_qk"], c["sigma_v"])
+
+    def dev_tensor(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    q, k, v = dev_tensor(qb), dev_tensor(kb), dev_tensor(vb)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    stream = torch.cuda.current_stream(dev)
+    sptr = int(stream.cuda_stream)
+
+    def step():
+        mha.mha_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, sptr)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    rc, word = mha.mha_device_status(sptr)
+    if rc != mha.MHA_OK:
+        raise RuntimeError(f"device status after warm-up: {rc} ({word:#x})")
+
+    # timed region: K launches, one event pair around each on the launch stream
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(dev.index) as clk:
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        evs[0].record(stream)
+        for i in range(args.steps):
+            step()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        if dist is not None:
+            dist.barrier()
+    per_launch_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    total_ms = evs[0].elapsed_time(evs[-1])
+    if dist is not None:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    rc, word = mha.mha_device_status(sptr)
+    if rc != mha.MHA_OK:
+        raise RuntimeError(f"device status after timing: {rc} ({word:#x})")
+
+    flops = counted_flops(c)
+    value = flops * args.steps * world / (total_ms / 1e3) / 1e12
+    mean_launch_ms = statistics.mean(per_launch_ms)
+    achieved = flops / (mean_launch_ms / 1e3) / 1e12
+    peak, peak_src = load_peaks()
+
+    # end to end through the public C ABI: pinned host inputs -> device ->
+    # mha_fwd -> O and LSE back to pinned host memory, every step
+    hq, hk, hv = (torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory()
+                  for b in (qb, kb, vb))
+    ho = torch.empty(o.shape, dtype=torch.bfloat16).pin_memory()
+    hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        step()
+        ho.copy_(o, non_blocking=True)
+        hl.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = flops * args.e2e_steps * world / (e2e_ms / 1e3) / 1e12
+    h2d = 3 * qb.nbytes
+    d2h = o.numel() * 2 + lse.numel() * 4
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        rows = size_oracle_sample(c, qb, kb, vb, 15.0)
+        dt, fl, nr = oracle_sample(c, qb, kb, vb, rows, [0])
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{nr} evenly spaced query rows of head 0, fp64, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": workload_name(name, c), "B": B, "H": H, "N": N, "d": d,
+                       "causal": causal, "seed": c["seed"], "flops_per_step": flops,
+                       "l2": "inputs larger than L2 (Q+K+V+O = %.0f MB > 129 MB)"
+                             % (4 * qb.nbytes / 1e6) if 4 * qb.nbytes > 129e6 else "no flush; inputs fit L2",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                         "frac": achieved / peak, "peak_source": peak_src,
+                         "traffic": recorded_traffic(name),
+                         "kernel": f"mha_fwd_kernel<{d},{'true' if causal else 'false'}>"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,18 @@
+"""Fused multi-head attention forward for NVIDIA GB300 (sm_103a).
+
+The compute runs in hand-written CUDA (``csrc/``) behind the C ABI of
+``include/mha_fwd.h``; this package only builds that library and binds its
+entry points with ctypes.
+"""
+from ._binding import (MHA_ERR_CUDA, MHA_ERR_INVALID_ARG, MHA_ERR_MISALIGNED, MHA_ERR_NO_DEVICE,
+                       MHA_ERR_TIMEOUT, MHA_ERR_UNSUPPORTED_DIM, MHA_OK, MhaError, forward, lib,
+                       mha_device_status, mha_fwd, mha_set_wait_limit, mha_strerror,
+                       mha_wait_selftest)
+from .build import LIB, build
+
+__all__ = [
+    "MHA_OK", "MHA_ERR_INVALID_ARG", "MHA_ERR_UNSUPPORTED_DIM", "MHA_ERR_MISALIGNED",
+    "MHA_ERR_CUDA", "MHA_ERR_TIMEOUT", "MHA_ERR_NO_DEVICE", "MhaError", "forward", "lib",
+    "mha_device_status", "mha_fwd", "mha_set_wait_limit", "mha_strerror", "mha_wait_selftest",
+    "LIB", "build",
+]

@@ -1,0 +1,244 @@
+// mha_fwd.cu - host side of the attention library: argument checks, TMA
+// tensor maps, launch configuration and the extern "C" entry points that
+// include/mha_fwd.h declares.
+//
+// The library links the CUDA runtime statically and reaches the one driver
+// entry point it needs (cuTensorMapEncodeTiled) through the runtime, so the
+// shared object loads on machines without a GPU driver; every entry point
+// validates its arguments before touching CUDA.
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "mha_fwd.h"
+#include "mha_fwd_kernel.cuh"
+
+namespace {
+
+// One status word per device (module memory, not an allocation).
+__device__ unsigned g_status;
+
+constexpr int kMaxDevices = 64;
+constexpr long long kDefaultWaitLimit = 1ll << 31;
+
+std::mutex g_mu;
+long long g_wait_limit = kDefaultWaitLimit;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+struct DeviceState {
+  bool ready = false;
+  bool ok = false;
+  unsigned* status = nullptr;
+};
+DeviceState g_dev[kMaxDevices];
+
+// Per-device set-up, done once under the lock: check the architecture,
+// raise the dynamic shared-memory limit of every kernel instantiation and
+// look up the status word's device address.
+int device_setup(int* dev_out, unsigned** status_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MHA_ERR_NO_DEVICE;
+  if (dev < 0 || dev >= kMaxDevices) return MHA_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.ready) {
+    st.ready = true;
+    st.ok = false;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      st.ready = false;
+      return MHA_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return MHA_ERR_NO_DEVICE;
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr) {
+        st.ready = false;
+        return MHA_ERR_CUDA;
+      }
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    bool fail = false;
+    fail |= cudaFuncSetAttribute(mha::mha_fwd_kernel<64, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mha::FwdCfg<64>::kSmemBytes) != cudaSuccess;
+    fail |= cudaFuncSetAttribute(mha::mha_fwd_kernel<64, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mha::FwdCfg<64>::kSmemBytes) != cudaSuccess;
+    fail |= cudaFuncSetAttribute(mha::mha_fwd_kernel<128, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mha::FwdCfg<128>::kSmemBytes) != cudaSuccess;
+    fail |= cudaFuncSetAttribute(mha::mha_fwd_kernel<128, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 mha::FwdCfg<128>::kSmemBytes) != cudaSuccess;
+    void* sym = nullptr;
+    fail |= cudaGetSymbolAddress(&sym, g_status) != cudaSuccess;
+    if (fail) {
+      st.ready = false;
+      return MHA_ERR_CUDA;
+    }
+    st.status = static_cast<unsigned*>(sym);
+    st.ok = true;
+  }
+  if (!st.ok) return MHA_ERR_NO_DEVICE;
+  *dev_out = dev;
+  *status_out = st.status;
+  return MHA_OK;
+}
+
+// 3-D view [BH][N][d] of a contiguous bf16 tensor; box = 64 x 128 x 1 with
+// the 128-byte swizzle the MMA descriptors expect.  Rows past N read as 0.
+bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int D, bool CAUSAL>
+cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                   const mha::FwdParams& prm, int BH, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(BH), static_cast<unsigned>(prm.num_mblocks), 1);
+  cfg.blockDim = dim3(mha::FwdCfg<D>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = mha::FwdCfg<D>::kSmemBytes;
+  cfg.stream = stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, mha::mha_fwd_kernel<D, CAUSAL>, mq, mk, mv, prm);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mha_strerror(int status) {
+  switch (status) {
+    case MHA_OK: return "ok";
+    case MHA_ERR_INVALID_ARG: return "invalid argument";
+    case MHA_ERR_UNSUPPORTED_DIM: return "unsupported head dimension (d must be 64 or 128)";
+    case MHA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case MHA_ERR_CUDA: return "CUDA call failed";
+    case MHA_ERR_TIMEOUT: return "device-side wait timed out";
+    case MHA_ERR_NO_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+            int d, float scale, int causal, void* stream) {
+  if (B < 0 || H < 0 || N < 0) return MHA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return MHA_ERR_UNSUPPORTED_DIM;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return MHA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH == 0 || N == 0) return MHA_OK;
+  if (BH > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return MHA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return MHA_ERR_MISALIGNED;
+  // the outputs must not overlap the inputs
+  const uintptr_t tb = static_cast<uintptr_t>(BH) * N * d * 2;
+  const uintptr_t lb = static_cast<uintptr_t>(BH) * N * 4;
+  auto overlap = [](const void* a, uintptr_t na, const void* b, uintptr_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+  };
+  for (const void* in : {q, k, v})
+    if (overlap(o, tb, in, tb) || overlap(lse, lb, in, tb)) return MHA_ERR_INVALID_ARG;
+  if (overlap(o, tb, lse, lb)) return MHA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  unsigned* status = nullptr;
+  const int rc = device_setup(&dev, &status);
+  if (rc != MHA_OK) return rc;
+
+  CUtensorMap mq, mk, mv;
+  if (!encode_map(&mq, q, static_cast<int>(BH), N, d) ||
+      !encode_map(&mk, k, static_cast<int>(BH), N, d) ||
+      !encode_map(&mv, v, static_cast<int>(BH), N, d))
+    return MHA_ERR_CUDA;
+
+  mha::FwdParams prm;
+  prm.o = static_cast<__nv_bfloat16*>(o);
+  prm.lse = lse;
+  prm.status = status;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    prm.wait_limit = g_wait_limit;
+  }
+  prm.N = N;
+  prm.num_mblocks = (N + 255) / 256;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t err;
+  if (d == 64)
+    err = causal ? launch<64, true>(mq, mk, mv, prm, static_cast<int>(BH), st)
+                 : launch<64, false>(mq, mk, mv, prm, static_cast<int>(BH), st);
+  else
+    err = causal ? launch<128, true>(mq, mk, mv, prm, static_cast<int>(BH), st)
+                 : launch<128, false>(mq, mk, mv, prm, static_cast<int>(BH), st);
+  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+int mha_device_status(void* stream, int reset, unsigned* detail) {
+  int dev = 0;
+  unsigned* status = nullptr;
+  const int rc = device_setup(&dev, &status);
+  if (rc != MHA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MHA_ERR_CUDA;
+  if (cudaMemcpy(&word, status, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MHA_ERR_CUDA;
+  if (reset && word != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MHA_ERR_CUDA;
+  }
+  if (detail) *detail = word;
+  return (word & mha::kStatusTimeout) ? MHA_ERR_TIMEOUT : MHA_OK;
+}
+
+int mha_set_wait_limit(long long cycles) {
+  if (cycles <= 0) return MHA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_wait_limit = cycles;
+  return MHA_OK;
+}
+
+int mha_wait_selftest(long long cycles, void* stream) {
+  if (cycles <= 0 || cycles > (1ll << 34)) return MHA_ERR_INVALID_ARG;
+  int dev = 0;
+  unsigned* status = nullptr;
+  int rc = device_setup(&dev, &status);
+  if (rc != MHA_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = st;
+  if (cudaLaunchKernelEx(&cfg, mha::wait_selftest_kernel, status, cycles) != cudaSuccess)
+    return MHA_ERR_CUDA;
+  unsigned word = 0;
+  rc = mha_device_status(stream, 1, &word);
+  if (rc == MHA_ERR_TIMEOUT && (word & mha::kSiteSelftest) == 0) return MHA_ERR_CUDA;
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,487 @@
+// mha_fwd_kernel.cuh - fused attention forward for sm_103a (GB300).
+//
+// What it computes: the FlashAttention-2 forward pass of the ML-Triton paper
+// (section 2.5, Algorithm 1): for a tile of queries, loop over key/value
+// tiles, S = Q K^T, online softmax with running row max m and row sum l,
+// O += P V, and one final normalisation.  The running statistics follow the
+// Triton-learning blog (Puzzle 8: sum' = sum * exp(m1 - m2) + sum exp(x - m2);
+// Puzzle 9: the output is rescaled by the same factor), with the division by
+// l deferred to the end, and exp written as exp2 of a pre-scaled argument
+// (blog, Puzzle 8: exp(x) = 2^(log2(e) x)).
+//
+// How it maps to GB300 (one CTA = 256 query rows of one (batch, head)):
+//   warp 0      TMA producer: Q0/Q1 once, then K_j / V_j into a ring of
+//               shared-memory stages guarded by full/empty mbarriers (the
+//               producer/consumer tokens of the Triton warp-specialisation
+//               notes: acquire -> expect bytes -> TMA copy; consumer waits
+//               -> uses -> releases).
+//   warp 1      MMA issuer (one thread): S_j(s) = Q_s K_j^T with
+//               tcgen05.mma into TMEM, then O(s) += P_j(s) V_j with P read
+//               straight from TMEM.  Also allocates / frees TMEM.
+//   warps 4-7   softmax warpgroup for Q tile 0 (TMEM lanes 0-127, one query
+//   warps 8-11  row per thread), softmax warpgroup for Q tile 1.  Each reads
+//               its S row from TMEM, masks, updates m and l, writes P (bf16)
+//               back over S, rescales O in TMEM when its max moved (the
+//               correction stage), and finally writes O / l and the LSE.
+//   warps 2-3   idle (keep the softmax warpgroups aligned to TMEM lanes).
+// The two Q tiles ping-pong: while one softmax warpgroup works on its S, the
+// tensor core runs the other tile's GEMMs (the cooperative M-split of the
+// warp-specialisation notes, one consumer group per half of the rows).
+//
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
+// P_j(s) (128 keys as 64 packed bf16x2 columns) overwrites S(s) cols [0,64).
+// The tensor pipe executes one thread's MMAs in issue order, so issuing
+// S_{j+1}(s) after PV_j(s) cannot clobber P_j(s) before it is read.
+//
+// Every mbarrier wait is bounded (clock64 budget).  A wait that runs out
+// records a code in the device status word, raises a CTA-wide abort flag
+// that ends every other wait at once, and the CTA then drains its own
+// in-flight copies and MMAs (again with a bound) and frees TMEM.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace mha {
+
+// Bits of the device status word.
+constexpr unsigned kStatusTimeout = 1u << 31;
+enum WaitSite : unsigned {
+  kSiteProducerEmpty = 1u << 0,
+  kSiteMmaQ = 1u << 1,
+  kSiteMmaKV = 1u << 2,
+  kSiteMmaP = 1u << 3,
+  kSiteSoftmaxS = 1u << 4,
+  kSiteSoftmaxO = 1u << 5,
+  kSiteDrain = 1u << 6,
+  kSiteSelftest = 1u << 7,
+};
+
+struct FwdParams {
+  __nv_bfloat16* o;    // [BH, N, D]
+  float* lse;          // [BH, N]
+  unsigned* status;    // device status word
+  long long wait_limit;  // SM cycles per wait
+  int N;
+  int num_mblocks;     // ceil(N / 256)
+  float scale_log2;    // scale * log2(e)
+};
+
+template <int D>
+struct FwdCfg {
+  static_assert(D == 64 || D == 128, "head dimension");
+  static constexpr int kBlockM = 128;  // query rows per softmax warpgroup
+  static constexpr int kBlockN = 128;  // keys per K/V tile
+  static constexpr int kHalves = D / 64;  // 128-byte swizzle atoms across d
+  static constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kStages = (D == 128) ? 4 : 8;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  // barriers: q_full[2] kv_full[S] kv_empty[S] s_full[2] p_ready[2] o_full[2] drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
+  static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
+  static constexpr int kThreads = 384;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
+  // the running max only moves (and O is only rescaled) once it has grown
+  // by more than this many powers of two; P stays <= 2^8 meanwhile.
+  static constexpr float kRescaleThreshold = 8.0f;
+};
+
+struct WaitCtl {
+  volatile int* abort;
+  unsigned* status;
+  long long limit;
+};
+
+__device__ __forceinline__ void raise_timeout(const WaitCtl& c, unsigned site) {
+  *c.abort = 1;
+  atomicOr(c.status, kStatusTimeout | site);
+}
+
+// Bounded wait by a single thread.  Returns false on abort or timeout.
+__device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                         unsigned site) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (*c.abort) return false;
+    if (clock64() - t0 > c.limit) {
+      raise_timeout(c, site);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Bounded wait by a whole warp, with a warp-uniform outcome (the warp goes
+// on to execute .sync.aligned tcgen05 instructions together).
+__device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c,
+                                          unsigned site) {
+  const long long t0 = clock64();
+  while (true) {
+    const uint32_t ok = ptx::mbar_try_wait(bar, parity);
+    if (__all_sync(0xffffffffu, ok)) return true;
+    int stop = 0;
+    if ((threadIdx.x & 31) == 0) {
+      if (*c.abort)
+        stop = 1;
+      else if (clock64() - t0 > c.limit)
+        stop = 2;
+    }
+    stop = __shfl_sync(0xffffffffu, stop, 0);
+    if (stop) {
+      if (stop == 2 && (threadIdx.x & 31) == 0) raise_timeout(c, site);
+      return false;
+    }
+  }
+}
+
+// Wait with its own budget that ignores the abort flag: used only to drain
+// copies / MMAs this CTA started before it frees its resources.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const WaitCtl& c) {
+  const long long t0 = clock64();
+  while (!ptx::mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > c.limit) {
+      atomicOr(c.status, kStatusTimeout | kSiteDrain);
+      return;
+    }
+  }
+}
+
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+    mha_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int mblk = CAUSAL ? (p.num_mblocks - 1 - static_cast<int>(blockIdx.y))
+                          : static_cast<int>(blockIdx.y);
+  const int m0 = mblk * 256;
+  const int N = p.N;
+  const int n_tiles = (N + C::kBlockN - 1) / C::kBlockN;
+  // K/V tiles each Q tile needs (0 when the Q tile lies past the end).
+  int n_s[2];
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    const int row0 = m0 + s * C::kBlockM;
+    n_s[s] = row0 >= N ? 0 : (CAUSAL ? min(n_tiles, row0 / C::kBlockN + 1) : n_tiles);
+  }
+  const int n_kv = max(n_s[0], n_s[1]);
+
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
+  auto q_full = [&](int s) { return bar(s); };
+  auto kv_full = [&](int i) { return bar(2 + i); };
+  auto kv_empty = [&](int i) { return bar(2 + C::kStages + i); };
+  auto s_full = [&](int s) { return bar(2 + 2 * C::kStages + s); };
+  auto p_ready = [&](int s) { return bar(4 + 2 * C::kStages + s); };
+  auto o_full = [&](int s) { return bar(6 + 2 * C::kStages + s); };
+  const uint32_t drain_bar = bar(8 + 2 * C::kStages);
+  auto sQ = [&](int s) -> uint32_t { return sbase + C::kOffQ + s * C::kTileBytes; };
+  auto sKV = [&](int i) -> uint32_t { return sbase + C::kOffKV + i * C::kTileBytes; };
+
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
+  const WaitCtl ctl{abort_flag, p.status, p.wait_limit};
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(q_full(0), 1);
+    ptx::mbar_init(q_full(1), 1);
+    for (int i = 0; i < C::kStages; ++i) {
+      ptx::mbar_init(kv_full(i), 1);
+      ptx::mbar_init(kv_empty(i), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(s_full(s), 1);
+      ptx::mbar_init(p_ready(s), 4 * 32);
+      ptx::mbar_init(o_full(s), 1);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&tmQ);
+    ptx::prefetch_tensormap(&tmK);
+    ptx::prefetch_tensormap(&tmV);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int s = 0; s < 2; ++s) {
+        if (n_s[s] == 0) continue;
+        ptx::mbar_arrive_expect_tx(q_full(s), C::kTileBytes);
+        for (int h = 0; h < C::kHalves; ++h)
+          ptx::tma_load_3d(sQ(s) + h * C::kHalfBytes, &tmQ, q_full(s), h * 64,
+                           m0 + s * C::kBlockM, bh);
+      }
+      int t = 0;  // ring position: K_j is load 2j, V_j is load 2j + 1
+      bool ok = true;
+      for (int j = 0; j < n_kv && ok; ++j) {
+        for (int which = 0; which < 2; ++which, ++t) {
+          const int slot = t % C::kStages;
+          const int use = t / C::kStages;
+          if (use > 0 && !wait_one(kv_empty(slot), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
+          const CUtensorMap* map = which ? &tmV : &tmK;
+          for (int h = 0; h < C::kHalves; ++h)
+            ptx::tma_load_3d(sKV(slot) + h * C::kHalfBytes, map, kv_full(slot), h * 64,
+                             j * C::kBlockN, bh);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA goes away
+        for (int s = 0; s < 2; ++s)
+          if (n_s[s] > 0) drain_wait(q_full(s), 0, ctl);
+        for (int u = max(0, t - C::kStages); u < t; ++u)
+          drain_wait(kv_full(u % C::kStages), (u / C::kStages) & 1, ctl);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, C::kBlockN, 0, 0);
+      constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(128, D, 0, 1);
+      const uint32_t colS[2] = {C::kColS0, C::kColS1};
+      const uint32_t colO[2] = {C::kColO0, C::kColO1};
+      bool ok = true;
+      for (int s = 0; s < 2 && ok; ++s)
+        if (n_s[s] > 0) ok = wait_one(q_full(s), 0, ctl, kSiteMmaQ);
+      int t = 0;
+      int v_prev = 0;
+      // O(s) += P_j(s) V_j : 128 keys in steps of 16; B = V tile, MN-major
+      // (d contiguous), d-halves LBO = 16 KiB apart, 8-key groups SBO = 1 KiB.
+      auto issue_pv = [&](int s, int jj, int vslot) {
+        for (int kk = 0; kk < C::kBlockN / 16; ++kk) {
+          const uint64_t bdesc = ptx::desc_sw128(sKV(vslot) + kk * 16 * 128, C::kHalfBytes, 1024);
+          ptx::mma_ts(tmem + colO[s], tmem + colS[s] + kk * 8, bdesc, kIdescO,
+                      (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+      };
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int k_slot = t % C::kStages, k_par = (t / C::kStages) & 1;
+        ++t;
+        const int v_slot = t % C::kStages, v_par = (t / C::kStages) & 1;
+        ++t;
+        if (!wait_one(kv_full(k_slot), k_par, ctl, kSiteMmaKV)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        for (int s = 0; s < 2 && ok; ++s) {
+          if (j >= 1 && j - 1 < n_s[s]) {
+            if (!wait_one(p_ready(s), (j - 1) & 1, ctl, kSiteMmaP)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_pv(s, j - 1, v_prev);
+            if (j - 1 == n_s[s] - 1) ptx::mma_commit(o_full(s));
+          }
+          if (j < n_s[s]) {
+            // S_j(s) = Q_s K_j^T : K = d in steps of 16, both operands
+            // K-major, 128-byte swizzled, 8-row groups SBO = 1 KiB apart.
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+              const uint64_t adesc = ptx::desc_sw128(sQ(s) + koff, 16, 1024);
+              const uint64_t bdesc = ptx::desc_sw128(sKV(k_slot) + koff, 16, 1024);
+              ptx::mma_ss(tmem + colS[s], adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
+            }
+            ptx::mma_commit(s_full(s));
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(kv_empty(k_slot));
+        if (j >= 1) ptx::mma_commit(kv_empty(v_prev));
+        if (!wait_one(kv_full(v_slot), v_par, ctl, kSiteMmaKV)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        v_prev = v_slot;
+      }
+      if (ok) {
+        for (int s = 0; s < 2 && ok; ++s) {
+          if (n_kv - 1 < n_s[s]) {
+            if (!wait_one(p_ready(s), (n_kv - 1) & 1, ctl, kSiteMmaP)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after();
+            issue_pv(s, n_kv - 1, v_prev);
+            ptx::mma_commit(o_full(s));
+          }
+        }
+        if (ok) ptx::mma_commit(kv_empty(v_prev));
+      }
+      // every MMA this thread issued completes before TMEM is released
+      ptx::mma_commit(drain_bar);
+      drain_wait(drain_bar, 0, ctl);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------- softmax / correction
+    const int s = (warp - 4) >> 2;
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = wq * 32 + lane;
+    const int q_idx = m0 + s * C::kBlockM + row;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + (s ? C::kColS1 : C::kColS0);
+    const uint32_t t_o = tmem + lane_off + (s ? C::kColO1 : C::kColO0);
+    const float sl2 = p.scale_log2;
+    const int n = n_s[s];
+    float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale
+    float l_run = 0.f;   // row sum of exp2 terms (fp32), for the LSE
+    float lr_run = 0.f;  // the same over the bf16-rounded terms, for O
+    bool ok = true;
+    for (int j = 0; j < n; ++j) {
+      if (!wait_warp(s_full(s), j & 1, ctl, kSiteSoftmaxS)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      uint32_t raw[128];
+      ptx::tmem_ld_x128(t_s, raw);
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(raw[c]);
+      const int kv0 = j * C::kBlockN;
+      const bool edge = (kv0 + C::kBlockN > N) || (CAUSAL && kv0 + C::kBlockN - 1 > m0 + s * C::kBlockM);
+      if (edge) {
+        const int lim = (CAUSAL ? min(N, q_idx + 1) : N) - kv0;  // keys [kv0, kv0+lim) visible
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) x[c] = -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = x[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+      const float tile_max =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_tile = tile_max * sl2;
+      float alpha = 1.f;
+      if (m_tile > m_run + C::kRescaleThreshold) {
+        alpha = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - m_tile);
+        m_run = m_tile;
+      }
+      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+      float sum[4] = {0.f, 0.f, 0.f, 0.f};   // of the fp32 p: for the LSE
+      float sumr[4] = {0.f, 0.f, 0.f, 0.f};  // of the bf16 p: for O / l
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ptx::ex2(fmaf(x[c4 * 32 + 2 * i], sl2, neg_m));
+          const float p1 = ptx::ex2(fmaf(x[c4 * 32 + 2 * i + 1], sl2, neg_m));
+          pk[i] = ptx::pack_bf16x2(p0, p1);
+          sum[i & 3] += p0 + p1;
+          // normalising O by the sum of the bf16 values the tensor core
+          // multiplies into V keeps O an exact convex combination of V rows
+          sumr[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+        }
+        ptx::tmem_st_x16(t_s + c4 * 16, pk);
+      }
+      l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      lr_run = lr_run * alpha + ((sumr[0] + sumr[1]) + (sumr[2] + sumr[3]));
+      // correction: bring O(s) to the new max before P_j(s) V_j lands on it
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          ptx::tmem_ld_x32(t_o + c * 32, ov);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          ptx::tmem_st_x32(t_o + c * 32, ov);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(p_ready(s));
+    }
+    if (ok && n > 0) {
+      if (wait_warp(o_full(s), 0, ctl, kSiteSoftmaxO)) {
+        ptx::tc_fence_after();
+        // epilogue: O = O_acc / l in bf16, LSE = (m + log2 l) * ln 2
+        const bool valid = q_idx < N;
+        const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
+        __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * N + (valid ? q_idx : 0)) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          ptx::tmem_ld_x32(t_o + c * 32, ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                     __uint_as_float(ov[2 * i + 1]) * inv_l);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        if (valid) {
+          const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
+          p.lse[static_cast<size_t>(bh) * N + q_idx] =
+              l_run > 0.f ? (m_fin + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// One warp waits, with the kernel's bounded wait, on a barrier nothing ever
+// completes; the wait must give up, record a timeout and return.
+__global__ void wait_selftest_kernel(unsigned* status, long long limit) {
+  __shared__ __align__(8) uint64_t bar_storage;
+  __shared__ int abort_flag;
+  const uint32_t b = ptx::smem_u32(&bar_storage);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(b, 1);
+    abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitCtl ctl{&abort_flag, status, limit};
+  wait_warp(b, 0, ctl, kSiteSelftest);
+  __syncwarp();
+}
+
+}  // namespace mha

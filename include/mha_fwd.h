@@ -1,0 +1,100 @@
+/*
+ * mha_fwd.h - fused multi-head attention forward pass for NVIDIA GB300
+ * (sm_103a), C ABI.
+ *
+ * The operation is the FlashAttention-2 forward pass: "two back-to-back
+ * GEMMs with an online softmax in between" (ML-Triton paper, section 2.5,
+ * Algorithm 1).  For every batch b, head h and query row i:
+ *
+ *     s_ij  = scale * <q_i, k_j>                 for j in J_i
+ *     J_i   = {0 .. N-1}, or {0 .. i} when causal != 0
+ *     O_i   = sum_j softmax(s_i)_j * v_j         (Triton-learning blog,
+ *                                                 Puzzle 9 definition)
+ *     LSE_i = ln sum_j exp(s_ij)                 (natural log)
+ *
+ * The row maximum and row sum are carried across key tiles with the online
+ * merge of the blog's Puzzle 8 and the output rescale of its Puzzle 9.
+ * S and P never reach global memory.
+ *
+ * Conventions shared by every entry point:
+ *   - Tensors are contiguous, row-major, and live in device memory.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) and returns once the work is queued.
+ *   - The caller allocates and owns every buffer.  The library allocates no
+ *     device memory; it keeps one status word per device in module memory.
+ *   - No call throws, aborts or exits.  A non-zero return means nothing
+ *     useful was written to the outputs.
+ */
+#ifndef MHA_FWD_H
+#define MHA_FWD_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    MHA_OK = 0,
+    MHA_ERR_INVALID_ARG = 1,     /* negative size, NULL pointer, bad scale   */
+    MHA_ERR_UNSUPPORTED_DIM = 2, /* head dimension d is not 64 or 128         */
+    MHA_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned          */
+    MHA_ERR_CUDA = 4,            /* a CUDA runtime or driver call failed      */
+    MHA_ERR_TIMEOUT = 5,         /* a device-side wait ran past its limit     */
+    MHA_ERR_NO_DEVICE = 6        /* no usable sm_103 device is current        */
+} mha_status;
+
+/*
+ * mha_fwd - attention forward pass.
+ *
+ *   q, k, v : bf16 [B, H, N, d], device, read only.
+ *   o       : bf16 [B, H, N, d], device, written (rounded to nearest even).
+ *   lse     : fp32 [B, H, N], device, written: LSE_i as defined above.
+ *   B, H, N : batch, heads, sequence length (queries = keys = N), each >= 0.
+ *             B*H*N == 0 is a no-op that returns MHA_OK.
+ *   d       : head dimension, 64 or 128.
+ *   scale   : score multiplier, finite and > 0 (usually 1/sqrt(d) in fp32).
+ *   causal  : 0 = every key; non-zero = key j > query i excluded (square,
+ *             top-left aligned mask).
+ *   stream  : cudaStream_t to launch on.
+ *
+ * All five pointers must be non-NULL and 16-byte aligned, and `o` / `lse`
+ * must not overlap the inputs.  Errors in the arguments are reported before
+ * any CUDA call.  MHA_ERR_CUDA reports a failed launch; faults that happen
+ * while the kernel runs surface at the caller's next synchronising CUDA call.
+ */
+int mha_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+            int B, int H, int N, int d, float scale, int causal, void *stream);
+
+/* A short, static, human-readable description of a status code. */
+const char *mha_strerror(int status);
+
+/*
+ * mha_device_status - synchronise `stream`, then read (and, if `reset` is
+ * non-zero, clear) the current device's status word, which records a
+ * device-side wait that ran out (every wait in the kernel is bounded).
+ * Returns MHA_OK, MHA_ERR_TIMEOUT, or MHA_ERR_CUDA if the read failed.
+ * `detail`, if non-NULL, receives the raw status word (0 when clean).
+ */
+int mha_device_status(void *stream, int reset, unsigned *detail);
+
+/*
+ * mha_set_wait_limit - set the cycle budget of every device-side wait for
+ * launches made after this call (default 2^31 SM cycles, about one second).
+ * `cycles` must be > 0.  Affects only this process.
+ */
+int mha_set_wait_limit(long long cycles);
+
+/*
+ * mha_wait_selftest - launch one block that waits, with the same bounded
+ * wait as the attention kernel, on a barrier that nothing completes, for
+ * at most `cycles` SM cycles; then synchronise `stream` and report.
+ * Returns MHA_ERR_TIMEOUT when the bounded wait gave up as designed (and
+ * clears the status word it set), MHA_OK if it did not.
+ */
+int mha_wait_selftest(long long cycles, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_FWD_H */

@@ -1,0 +1,90 @@
+"""The C ABI on a machine without a GPU: the library loads, exports every
+entry point include/mha_fwd.h declares, and rejects bad arguments before
+any CUDA call."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mha_fwd.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import head_attention_forward_gb300 as mha
+    mha.build()
+    return mha.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(mha_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert {"mha_fwd", "mha_strerror", "mha_device_status", "mha_set_wait_limit",
+            "mha_wait_selftest"} <= set(names)
+
+
+def test_every_declared_symbol_is_exported(L):
+    import head_attention_forward_gb300 as mha
+    out = subprocess.run(["nm", "-D", "--defined-only", mha.LIB], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in exported, name
+        getattr(L, name)
+
+
+def test_no_driver_dependency():
+    import head_attention_forward_gb300 as mha
+    out = subprocess.run(["ldd", mha.LIB], capture_output=True, text=True).stdout
+    assert "libcuda.so" not in out
+
+
+def _fwd(L, q=16, k=32, v=48, o=64, lse=80, B=1, H=1, N=4, d=64, scale=0.125, causal=0):
+    return L.mha_fwd(q, k, v, o, lse, B, H, N, d, ctypes.c_float(scale), causal, None)
+
+
+def test_argument_checks(L):
+    import head_attention_forward_gb300 as mha
+    big = 1 << 40  # far-apart fake addresses; never dereferenced
+    ok = dict(q=big, k=2 * big, v=3 * big, o=4 * big, lse=5 * big)
+    assert _fwd(L, **ok, d=96) == mha.MHA_ERR_UNSUPPORTED_DIM
+    assert _fwd(L, **ok, d=0) == mha.MHA_ERR_UNSUPPORTED_DIM
+    assert _fwd(L, **ok, B=-1) == mha.MHA_ERR_INVALID_ARG
+    assert _fwd(L, **ok, N=-5) == mha.MHA_ERR_INVALID_ARG
+    assert _fwd(L, **ok, scale=0.0) == mha.MHA_ERR_INVALID_ARG
+    assert _fwd(L, **ok, scale=float("inf")) == mha.MHA_ERR_INVALID_ARG
+    assert _fwd(L, **ok, scale=float("nan")) == mha.MHA_ERR_INVALID_ARG
+    assert _fwd(L, **dict(ok, q=0)) == mha.MHA_ERR_INVALID_ARG
+    assert _fwd(L, **dict(ok, lse=0)) == mha.MHA_ERR_INVALID_ARG
+    assert _fwd(L, **dict(ok, k=2 * big + 8)) == mha.MHA_ERR_MISALIGNED
+    assert _fwd(L, **dict(ok, o=big)) == mha.MHA_ERR_INVALID_ARG  # o aliases q
+    assert _fwd(L, **dict(ok, lse=2 * big + 64)) == mha.MHA_ERR_INVALID_ARG  # lse inside k
+    # empty problems return before any CUDA call
+    assert _fwd(L, **ok, N=0) == mha.MHA_OK
+    assert _fwd(L, **ok, B=0) == mha.MHA_OK
+    assert _fwd(L, q=0, k=0, v=0, o=0, lse=0, H=0) == mha.MHA_OK
+
+
+def test_other_entry_points_validate(L):
+    import head_attention_forward_gb300 as mha
+    assert L.mha_set_wait_limit(0) == mha.MHA_ERR_INVALID_ARG
+    assert L.mha_set_wait_limit(-3) == mha.MHA_ERR_INVALID_ARG
+    assert L.mha_wait_selftest(0, None) == mha.MHA_ERR_INVALID_ARG
+    for s in range(0, 8):
+        assert isinstance(mha.mha_strerror(s), str) and mha.mha_strerror(s)
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import head_attention_forward_gb300._binding as b
+    monkeypatch.setattr(b, "LIB", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(b, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        b.lib()

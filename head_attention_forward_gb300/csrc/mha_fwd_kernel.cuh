@@ -379,13 +379,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) x[c] = -INFINITY;
       }
+      // row maximum of this tile: 8 independent chains of 3-input max
       float mx[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx[i] = x[i];
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
-      const float tile_max =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 8; c < 128; c += 2) mx[(c >> 1) & 7] = ptx::max3(mx[(c >> 1) & 7], x[c], x[c + 1]);
+      const float tile_max = fmaxf(ptx::max3(mx[0], mx[1], mx[2]),
+                                   fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const float m_tile = tile_max * sl2;
       float alpha = 1.f;
       if (m_tile > m_run + C::kRescaleThreshold) {
@@ -393,24 +394,28 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         m_run = m_tile;
       }
       const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-      float sum[4] = {0.f, 0.f, 0.f, 0.f};   // of the fp32 p: for the LSE
-      float sumr[4] = {0.f, 0.f, 0.f, 0.f};  // of the bf16 p: for O / l
+      const float2 sl2v = make_float2(sl2, sl2);
+      const float2 negm = make_float2(neg_m, neg_m);
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // fp32 p: for the LSE
+      float sumr[4] = {0.f, 0.f, 0.f, 0.f};  // bf16 p: for O / l
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ptx::ex2(fmaf(x[c4 * 32 + 2 * i], sl2, neg_m));
-          const float p1 = ptx::ex2(fmaf(x[c4 * 32 + 2 * i + 1], sl2, neg_m));
+          const float2 t = __ffma2_rn(make_float2(x[c4 * 32 + 2 * i], x[c4 * 32 + 2 * i + 1]), sl2v, negm);
+          const float p0 = ptx::ex2(t.x);
+          const float p1 = ptx::ex2(t.y);
           pk[i] = ptx::pack_bf16x2(p0, p1);
-          sum[i & 3] += p0 + p1;
+          sum2[i & 1] = __fadd2_rn(sum2[i & 1], make_float2(p0, p1));
           // normalising O by the sum of the bf16 values the tensor core
           // multiplies into V keeps O an exact convex combination of V rows
-          sumr[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+          sumr[(2 * i) & 3] = ptx::add_bf16_lo(pk[i], sumr[(2 * i) & 3]);
+          sumr[(2 * i + 1) & 3] = ptx::add_bf16_hi(pk[i], sumr[(2 * i + 1) & 3]);
         }
         ptx::tmem_st_x16(t_s + c4 * 16, pk);
       }
-      l_run = l_run * alpha + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
       lr_run = lr_run * alpha + ((sumr[0] + sumr[1]) + (sumr[2] + sumr[3]));
       // correction: bring O(s) to the new max before P_j(s) V_j lands on it
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {

@@ -164,6 +164,30 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// c + (bf16 in bits 0..15 of pk), and c + (bf16 in bits 16..31 of pk), in
+// fp32: mixed-precision adds that widen the bf16 operand exactly.
+__device__ __forceinline__ float add_bf16_lo(uint32_t pk, float c) {
+  float d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, l, %2;\n\t}"
+      : "=f"(d)
+      : "r"(pk), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float add_bf16_hi(uint32_t pk, float c) {
+  float d;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %1;\n\tadd.rn.f32.bf16 %0, h, %2;\n\t}"
+      : "=f"(d)
+      : "r"(pk), "f"(c));
+  return d;
+}
+
 // Two floats -> packed bf16x2 (round to nearest even); `lo` in bits 0..15.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;

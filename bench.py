@@ -39,6 +39,7 @@ import synth  # noqa: E402
 METRIC = "attention fwd TFLOP/s and % of GB300 bf16 tensor peak, per (B,H,N,d,causal)"
 UNIT = "TFLOP/s"
 FALLBACK_PEAK_TFLOPS = 1900.0  # used only when MEASURED_PEAKS.json is absent
+FALLBACK_PEAK_SUSTAINED = 1700.0
 
 
 def counted_flops(c) -> float:
@@ -59,12 +60,20 @@ def host_cores() -> int:
 
 
 def load_peaks():
+    """(sustained, burst, source) dense bf16 peaks in TFLOP/s.
+
+    The timed region is hundreds of back-to-back launches (most of a second
+    under the board power cap), the situation of the sustained cuBLAS
+    measurement, so the roofline fraction uses the sustained figure; the
+    burst fraction is reported beside it."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             pk = json.load(f)
-        return float(pk["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
-    return FALLBACK_PEAK_TFLOPS, "fallback (no MEASURED_PEAKS.json)"
+        burst = float(pk["bf16_tflops"])
+        sustained = float(pk.get("bf16_tflops_sustained", burst))
+        return sustained, burst, "measured (MEASURED_PEAKS.json: bf16_tflops_sustained; burst beside it)"
+    return FALLBACK_PEAK_SUSTAINED, FALLBACK_PEAK_TFLOPS, "fallback (no MEASURED_PEAKS.json)"
 
 
 def kernel_source_hash() -> str:
@@ -297,7 +306,7 @@ def main():
     value = flops * args.steps * world / (total_ms / 1e3) / 1e12
     mean_launch_ms = statistics.mean(per_launch_ms)
     achieved = flops / (mean_launch_ms / 1e3) / 1e12
-    peak, peak_src = load_peaks()
+    peak, peak_burst, peak_src = load_peaks()
 
     # end to end through the public C ABI: pinned host inputs -> device ->
     # mha_fwd -> O and LSE back to pinned host memory, every step
@@ -354,8 +363,10 @@ def main():
                              % (4 * qb.nbytes / 1e6) if 4 * qb.nbytes > 129e6 else "no flush; inputs fit L2",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_peak": 100.0 * value / world / peak,
+            "pct_of_burst_peak": 100.0 * value / world / peak_burst,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "peak_source": peak_src,
+                         "peak_burst": peak_burst, "frac_burst": achieved / peak_burst,
                          "traffic": recorded_traffic(name),
                          "kernel": f"mha_fwd_kernel<{d},{'true' if causal else 'false'}>"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,

@@ -174,13 +174,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const int N = p.N;
   const int n_tiles = (N + C::kBlockN - 1) / C::kBlockN;
   // K/V tiles each Q tile needs (0 when the Q tile lies past the end).
-  int n_s[2];
-#pragma unroll
-  for (int s = 0; s < 2; ++s) {
-    const int row0 = m0 + s * C::kBlockM;
-    n_s[s] = row0 >= N ? 0 : (CAUSAL ? min(n_tiles, row0 / C::kBlockN + 1) : n_tiles);
-  }
-  const int n_kv = max(n_s[0], n_s[1]);
+  auto tiles_for = [&](int row0) {
+    return row0 >= N ? 0 : (CAUSAL ? min(n_tiles, row0 / C::kBlockN + 1) : n_tiles);
+  };
+  const int n_s0 = tiles_for(m0), n_s1 = tiles_for(m0 + C::kBlockM);
+  auto n_s = [&](int s) { return s ? n_s1 : n_s0; };
+  const int n_kv = max(n_s0, n_s1);
 
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
   auto q_full = [&](int s) { return bar(s); };
@@ -206,7 +205,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(s_full(s), 1);
-      ptx::mbar_init(p_ready(s), 4 * 32);
+      ptx::mbar_init(p_ready(s), 4);  // one elected arrive per softmax warp
       ptx::mbar_init(o_full(s), 1);
     }
     ptx::mbar_init(drain_bar, 1);
@@ -231,7 +230,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       for (int s = 0; s < 2; ++s) {
-        if (n_s[s] == 0) continue;
+        if (n_s(s) == 0) continue;
         ptx::mbar_arrive_expect_tx(q_full(s), C::kTileBytes);
         for (int h = 0; h < C::kHalves; ++h)
           ptx::tma_load_3d(sQ(s) + h * C::kHalfBytes, &tmQ, q_full(s), h * 64,
@@ -257,7 +256,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       if (!ok) {
         // let the copies already issued land before the CTA goes away
         for (int s = 0; s < 2; ++s)
-          if (n_s[s] > 0) drain_wait(q_full(s), 0, ctl);
+          if (n_s(s) > 0) drain_wait(q_full(s), 0, ctl);
         for (int u = max(0, t - C::kStages); u < t; ++u)
           drain_wait(kv_full(u % C::kStages), (u / C::kStages) & 1, ctl);
       }
@@ -268,22 +267,49 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, C::kBlockN, 0, 0);
       constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(128, D, 0, 1);
-      const uint32_t colS[2] = {C::kColS0, C::kColS1};
-      const uint32_t colO[2] = {C::kColO0, C::kColO1};
-      bool ok = true;
-      for (int s = 0; s < 2 && ok; ++s)
-        if (n_s[s] > 0) ok = wait_one(q_full(s), 0, ctl, kSiteMmaQ);
-      int t = 0;
-      int v_prev = 0;
-      // O(s) += P_j(s) V_j : 128 keys in steps of 16; B = V tile, MN-major
-      // (d contiguous), d-halves LBO = 16 KiB apart, 8-key groups SBO = 1 KiB.
-      auto issue_pv = [&](int s, int jj, int vslot) {
-        for (int kk = 0; kk < C::kBlockN / 16; ++kk) {
-          const uint64_t bdesc = ptx::desc_sw128(sKV(vslot) + kk * 16 * 128, C::kHalfBytes, 1024);
-          ptx::mma_ts(tmem + colO[s], tmem + colS[s] + kk * 8, bdesc, kIdescO,
-                      (jj > 0 || kk > 0) ? 1u : 0u);
+      const uint32_t tS0 = tmem + C::kColS0, tS1 = tmem + C::kColS1;
+      const uint32_t tO0 = tmem + C::kColO0, tO1 = tmem + C::kColO1;
+      // Descriptors are built once; moving to another slot or k-step only
+      // adds (byte offset >> 4) to the start-address field, which never
+      // carries out of it because every operand lies below 256 KiB.  The
+      // single issuing thread is the tensor core's only feeder, so keeping
+      // its per-MMA work to an add and the instruction itself matters.
+      // Q and K tiles: K-major, 128-byte swizzle, 8-row groups 1 KiB apart.
+      const uint64_t dQ0 = ptx::desc_sw128(sQ(0), 16, 1024), dQ1 = ptx::desc_sw128(sQ(1), 16, 1024);
+      const uint64_t dK0 = ptx::desc_sw128(sKV(0), 16, 1024);
+      // V tiles: MN-major (d contiguous), d-halves 16 KiB apart (LBO),
+      // 8-key groups 1 KiB apart (SBO).
+      const uint64_t dV0 = ptx::desc_sw128(sKV(0), C::kHalfBytes, 1024);
+      auto slot_off = [](int slot) -> uint64_t {
+        return static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
+      };
+      // S(s) = Q_s K^T over K = d in steps of 16
+      auto issue_s = [&](int s, int kslot) {
+        const uint64_t dk = dK0 + slot_off(kslot);
+        const uint64_t dq = s ? dQ1 : dQ0;
+        const uint32_t ts = s ? tS1 : tS0;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t koff =
+              static_cast<uint64_t>(((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4);
+          ptx::mma_ss(ts, dq + koff, dk + koff, kIdescS, kk > 0 ? 1u : 0u);
         }
       };
+      // O(s) += P(s) V over 128 keys in steps of 16; P read from TMEM
+      auto issue_pv = [&](int s, int vslot, bool first) {
+        const uint64_t dv = dV0 + slot_off(vslot);
+        const uint32_t ts = s ? tS1 : tS0;
+        const uint32_t to = s ? tO1 : tO0;
+#pragma unroll
+        for (int kk = 0; kk < C::kBlockN / 16; ++kk)
+          ptx::mma_ts(to, ts + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescO,
+                      (!first || kk > 0) ? 1u : 0u);
+      };
+      bool ok = true;
+      for (int s = 0; s < 2 && ok; ++s)
+        if (n_s(s) > 0) ok = wait_one(q_full(s), 0, ctl, kSiteMmaQ);
+      int t = 0;
+      int v_prev = 0;
       for (int j = 0; j < n_kv && ok; ++j) {
         const int k_slot = t % C::kStages, k_par = (t / C::kStages) & 1;
         ++t;
@@ -295,24 +321,17 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         ptx::tc_fence_after();
         for (int s = 0; s < 2 && ok; ++s) {
-          if (j >= 1 && j - 1 < n_s[s]) {
+          if (j >= 1 && j - 1 < n_s(s)) {
             if (!wait_one(p_ready(s), (j - 1) & 1, ctl, kSiteMmaP)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            issue_pv(s, j - 1, v_prev);
-            if (j - 1 == n_s[s] - 1) ptx::mma_commit(o_full(s));
+            issue_pv(s, v_prev, j - 1 == 0);
+            if (j - 1 == n_s(s) - 1) ptx::mma_commit(o_full(s));
           }
-          if (j < n_s[s]) {
-            // S_j(s) = Q_s K_j^T : K = d in steps of 16, both operands
-            // K-major, 128-byte swizzled, 8-row groups SBO = 1 KiB apart.
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-              const uint64_t adesc = ptx::desc_sw128(sQ(s) + koff, 16, 1024);
-              const uint64_t bdesc = ptx::desc_sw128(sKV(k_slot) + koff, 16, 1024);
-              ptx::mma_ss(tmem + colS[s], adesc, bdesc, kIdescS, kk > 0 ? 1u : 0u);
-            }
+          if (j < n_s(s)) {
+            issue_s(s, k_slot);
             ptx::mma_commit(s_full(s));
           }
         }
@@ -328,13 +347,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       }
       if (ok) {
         for (int s = 0; s < 2 && ok; ++s) {
-          if (n_kv - 1 < n_s[s]) {
+          if (n_kv - 1 < n_s(s)) {
             if (!wait_one(p_ready(s), (n_kv - 1) & 1, ctl, kSiteMmaP)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
-            issue_pv(s, n_kv - 1, v_prev);
+            issue_pv(s, v_prev, n_kv - 1 == 0);
             ptx::mma_commit(o_full(s));
           }
         }
@@ -355,7 +374,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t t_s = tmem + lane_off + (s ? C::kColS1 : C::kColS0);
     const uint32_t t_o = tmem + lane_off + (s ? C::kColO1 : C::kColO0);
     const float sl2 = p.scale_log2;
-    const int n = n_s[s];
+    const int n = n_s(s);
     float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale
     float l_run = 0.f;   // row sum of exp2 terms (fp32), for the LSE
     float lr_run = 0.f;  // the same over the bf16-rounded terms, for O
@@ -430,7 +449,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(p_ready(s));
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(p_ready(s));
     }
     if (ok && n > 0) {
       if (wait_warp(o_full(s), 0, ctl, kSiteSoftmaxO)) {

@@ -240,6 +240,7 @@ def main():
     import torch
 
     import head_attention_forward_gb300 as mha
+    from head_attention_forward_gb300.sharding import replica_seed
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -256,7 +257,7 @@ def main():
     mha.lib()
 
     B, H, N, d, causal = c["B"], c["H"], c["N"], c["d"], c["causal"]
-    seed = c["seed"] + 1000 * rank
+    seed = replica_seed(c["seed"], rank)
     qb, kb, vb = synth.qkv(seed, B, H, N, d, c["sigma_qk"], c["sigma_v"])
 
     def dev_tensor(bits):

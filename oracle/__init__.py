@@ -52,6 +52,9 @@ def _load():
                                                p, p, p]
         lib.oracle_attention_probs.restype = ctypes.c_int
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_attention_kv.argtypes = [p, p, p, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                            p, p, ctypes.c_int]
+        lib.oracle_attention_kv.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -120,3 +123,34 @@ def attention_probs(q, k, v, scale: float, causal: bool):
     if rc != 0:
         raise RuntimeError("oracle_attention_probs failed")
     return p, o, lse
+
+
+def attention_kv(q, k, v, scale: float, causal: bool, nthreads: int = 0):
+    """Nq queries against Nk keys: q [B,H,Nq,d], k/v [B,H,Nk,d] bf16 bits.
+
+    Causal here is bottom-right aligned (the queries are the last Nq
+    positions): query i sees keys 0 .. Nk-Nq+i.  Returns O [B,H,Nq,d] and
+    LSE [B,H,Nq] in float64.
+    """
+    q, k, v = _bits(q), _bits(k), _bits(v)
+    if q.ndim != 4 or k.shape != v.shape or q.shape[:2] != k.shape[:2] or q.shape[3] != k.shape[3]:
+        raise ValueError("q [B,H,Nq,d] and k, v [B,H,Nk,d] expected")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    o = np.zeros((B, H, Nq, d), dtype=np.float64)
+    lse = np.zeros((B, H, Nq), dtype=np.float64)
+    lib = _load()
+    for bh in range(B * H):
+        b, h = divmod(bh, H)
+        qb = np.ascontiguousarray(q[b, h])
+        kb = np.ascontiguousarray(k[b, h])
+        vb = np.ascontiguousarray(v[b, h])
+        ob = np.zeros((Nq, d), dtype=np.float64)
+        lb = np.zeros(Nq, dtype=np.float64)
+        rc = lib.oracle_attention_kv(_ptr(qb), _ptr(kb), _ptr(vb), Nq, Nk, d, ctypes.c_float(scale),
+                                     int(bool(causal)), _ptr(ob), _ptr(lb), int(nthreads))
+        if rc != 0:
+            raise RuntimeError("oracle_attention_kv failed")
+        o[b, h] = ob
+        lse[b, h] = lb
+    return o, lse

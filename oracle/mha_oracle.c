@@ -38,15 +38,14 @@ static double bf16_to_f64(uint16_t b) {
     return (double)f;
 }
 
-/* One query row i of one head.  q_bh, k_bh, v_bh: [N, d] bf16 bits.
- * s: scratch of N doubles.  o_row: d doubles out.  p_row: optional N
- * doubles out (the softmax probabilities; zero for keys outside J_i). */
-static void attention_row(const uint16_t *q_bh, const uint16_t *k_bh, const uint16_t *v_bh,
-                          int64_t N, int64_t d, double scale, int causal, int64_t i,
-                          double *s, double *o_row, double *lse, double *p_row) {
-    /* key set J_i = {0..N-1}, or {0..i} under the causal mask */
-    int64_t nk = causal ? i + 1 : N;
-    if (nk > N) nk = N;
+/* One query row of one head over the keys 0..nk-1 (its key set J_i).
+ * q_row: [d] bf16 bits; k_bh, v_bh: [Nk, d] bf16 bits.  s: scratch of at
+ * least nk doubles.  o_row: d doubles out.  p_row: optional Nk doubles out
+ * (the softmax probabilities; zero for keys outside J_i). */
+static void attention_row_keys(const uint16_t *q_row, const uint16_t *k_bh, const uint16_t *v_bh,
+                               int64_t Nk, int64_t d, double scale, int64_t nk,
+                               double *s, double *o_row, double *lse, double *p_row) {
+    const int64_t N = Nk;
     for (int64_t c = 0; c < d; ++c) o_row[c] = 0.0;
     if (p_row)
         for (int64_t j = 0; j < N; ++j) p_row[j] = 0.0;
@@ -58,7 +57,7 @@ static void attention_row(const uint16_t *q_bh, const uint16_t *k_bh, const uint
     for (int64_t j = 0; j < nk; ++j) {
         double acc = 0.0;
         for (int64_t c = 0; c < d; ++c)
-            acc += bf16_to_f64(q_bh[i * d + c]) * bf16_to_f64(k_bh[j * d + c]);
+            acc += bf16_to_f64(q_row[c]) * bf16_to_f64(k_bh[j * d + c]);
         s[j] = scale * acc;
     }
     /* row maximum and the sum of shifted exponentials */
@@ -74,6 +73,16 @@ static void attention_row(const uint16_t *q_bh, const uint16_t *k_bh, const uint
         for (int64_t c = 0; c < d; ++c) o_row[c] += p * bf16_to_f64(v_bh[j * d + c]);
     }
     *lse = m + log(l);
+}
+
+/* Square case: query i of N sees keys {0..N-1}, or {0..i} under the causal
+ * mask (top-left aligned). */
+static void attention_row(const uint16_t *q_bh, const uint16_t *k_bh, const uint16_t *v_bh,
+                          int64_t N, int64_t d, double scale, int causal, int64_t i,
+                          double *s, double *o_row, double *lse, double *p_row) {
+    int64_t nk = causal ? i + 1 : N;
+    if (nk > N) nk = N;
+    attention_row_keys(q_bh + i * d, k_bh, v_bh, N, d, scale, nk, s, o_row, lse, p_row);
 }
 
 /* Rows rows[0..nrows-1] of one head.  o_out: [nrows, d]; lse_out: [nrows].
@@ -148,4 +157,39 @@ int oracle_num_threads(void) {
 #else
     return 1;
 #endif
+}
+
+/* Nq queries against Nk keys of one head (q_bh [Nq, d], k_bh / v_bh
+ * [Nk, d]).  Under the causal mask the queries are the last Nq positions of
+ * the sequence (bottom-right aligned): query i sees keys 0 .. Nk-Nq+i, and
+ * none when that bound is negative.  With Nq == Nk this is the square case. */
+int oracle_attention_kv(const uint16_t *q_bh, const uint16_t *k_bh, const uint16_t *v_bh,
+                        int64_t Nq, int64_t Nk, int64_t d, float scale, int causal,
+                        double *o_out, double *lse_out, int nthreads) {
+    if (Nq < 0 || Nk < 0 || d <= 0) return -1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#else
+    nthreads = 1;
+#endif
+    int bad = 0;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)(Nk > 0 ? Nk : 1));
+        if (!s) {
+#pragma omp atomic write
+            bad = 1;
+        } else {
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t i = 0; i < Nq; ++i) {
+                int64_t nk = causal ? Nk - Nq + i + 1 : Nk;
+                if (nk < 0) nk = 0;
+                if (nk > Nk) nk = Nk;
+                attention_row_keys(q_bh + i * d, k_bh, v_bh, Nk, d, (double)scale, nk, s,
+                                   o_out + i * d, lse_out + i, NULL);
+            }
+            free(s);
+        }
+    }
+    return bad ? -1 : 0;
 }

@@ -240,3 +240,58 @@ def test_mask_is_square_top_left():
         o2, _ = oracle.attention_fwd(q, k, v2, 0.5, True)
         assert np.array_equal(o2[0, 0, : i + 1], o[0, 0, : i + 1])
         assert not np.array_equal(o2[0, 0, i + 1], o[0, 0, i + 1])
+
+
+# ------------------------------------------- Nq queries against Nk keys
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_square_case_is_the_square_oracle(causal):
+    q, k, v = synth.qkv(31, 1, 2, 37, 16, compiled=False)
+    o1, l1 = oracle.attention_fwd(q, k, v, 0.25, causal)
+    o2, l2 = oracle.attention_kv(q, k, v, 0.25, causal)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_kv_last_queries_match_square_rows():
+    """The last Nq rows of a square causal problem are exactly the
+    bottom-right aligned Nq-query problem over the same keys."""
+    N, d, nq = 45, 8, 5
+    q, k, v = synth.qkv(32, 1, 2, N, d, compiled=False)
+    o1, l1 = oracle.attention_fwd(q, k, v, 0.5, True)
+    o2, l2 = oracle.attention_kv(np.ascontiguousarray(q[:, :, N - nq:]), k, v, 0.5, True)
+    assert np.array_equal(o2, o1[:, :, N - nq:]) and np.array_equal(l2, l1[:, :, N - nq:])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_kv_brute_force(causal):
+    r = random.Random(9 + causal)
+    for trial in range(4):
+        nq, nk, d = r.randint(1, 6), r.randint(1, 9), r.randint(1, 6)
+        q = rand_bits(200 + trial, (1, 1, nq, d))
+        k, v = rand_bits(210 + trial, (1, 1, nk, d)), rand_bits(220 + trial, (1, 1, nk, d))
+        scale = float(np.float32(0.7))  # the oracle takes the scale as fp32
+        o, lse = oracle.attention_kv(q, k, v, scale, causal)
+        qf, kf, vf = f64(q)[0, 0], f64(k)[0, 0], f64(v)[0, 0]
+        for i in range(nq):
+            keys = list(range(min(nk, nk - nq + i + 1))) if causal else list(range(nk))
+            if not keys:
+                assert np.all(o[0, 0, i] == 0) and lse[0, 0, i] == -np.inf
+                continue
+            w = [math.exp(scale * math.fsum(qf[i][c] * kf[j][c] for c in range(d))) for j in keys]
+            tot = math.fsum(w)
+            ref = [math.fsum(w[t] * vf[j][c] for t, j in enumerate(keys)) / tot for c in range(d)]
+            np.testing.assert_allclose(o[0, 0, i], ref, rtol=0, atol=1e-12)
+            assert abs(lse[0, 0, i] - math.log(tot)) < 1e-12
+
+
+def test_kv_torch_sdpa_bottom_right():
+    torch = pytest.importorskip("torch")
+    nq, nk, d = 6, 50, 32
+    q = rand_bits(301, (2, 2, nq, d))
+    k, v = rand_bits(302, (2, 2, nk, d)), rand_bits(303, (2, 2, nk, d))
+    o, lse = oracle.attention_kv(q, k, v, 0.125, True)
+    mask = torch.ones(nq, nk, dtype=torch.bool).tril(nk - nq)
+    tq, tk, tv = (torch.from_numpy(f64(a)) for a in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=mask, scale=0.125)
+    np.testing.assert_allclose(o, ref.numpy(), rtol=0, atol=1e-12)
+    s = (0.125 * tq @ tk.transpose(-1, -2)).masked_fill(~mask, float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)

@@ -220,17 +220,111 @@ def run_reference(args, c, name):
     return 0
 
 
+def run_decode(args, name):
+    """Split-KV path on a decode-shaped workload (single GPU): TFLOP/s with
+    the same counting rule, plus the HBM roofline, which bounds this path."""
+    import torch
+
+    import head_attention_forward_gb300 as mha
+    c = synth.DECODE_CONFIGS[name]
+    B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
+    qb, kb, vb = synth.decode_inputs(name)
+    if args.impl == "reference":
+        import oracle
+        heads = 1
+        t0 = time.perf_counter()
+        oracle.attention_kv(qb[:1, :heads], kb[:1, :heads], vb[:1, :heads],
+                            float(np.float32(1 / math.sqrt(d))), causal)
+        dt = time.perf_counter() - t0
+        fl = 4.0 * heads * Nq * Nk * d
+        print(json.dumps({"impl": "reference", "metric": METRIC, "value": fl / dt / 1e12, "unit": UNIT,
+                          "n_gpus": 0, "steps": 1, "warmup": 0, "ms_per_step": dt * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                          "dtype": "f64", "data": "synthetic",
+                          "config": {"workload": f"{name}: B={B},H={H},Nq={Nq},Nk={Nk},d={d}"},
+                          "cpu_baseline": {"value": fl / dt / 1e12, "unit": UNIT,
+                                           "cores": oracle.num_threads(), "kind": "oracle",
+                                           "sample": f"{heads} head(s) of the workload"},
+                          "e2e": {"value": fl / dt / 1e12, "unit": UNIT, "h2d_bytes_per_step": 0,
+                                  "d2h_bytes_per_step": 0}}), flush=True)
+        return 0
+    torch.cuda.set_device(0)
+    mha.build()
+    mha.lib()
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v = dev(qb), dev(kb), dev(vb)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, Nk, d, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    stream = torch.cuda.current_stream()
+    sptr = int(stream.cuda_stream)
+
+    def step():
+        mha.mha_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 0, ws, ws_bytes, sptr)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        evs[0].record(stream)
+        for i in range(args.steps):
+            step()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+    rc, word = mha.mha_device_status(sptr)
+    if rc != mha.MHA_OK:
+        raise RuntimeError(f"device status {rc} ({word:#x})")
+    total_ms = evs[0].elapsed_time(evs[-1])
+    ms = total_ms / args.steps
+    # FLOPs: 4 Nq Nk d per head (every key visible to the newest query)
+    flops = 4.0 * B * H * Nq * Nk * d
+    algo_bytes = 2 * (q.numel() + k.numel() + v.numel() + o.numel()) + 4 * lse.numel()
+    gbs = algo_bytes / (ms / 1e3) / 1e9
+    hbm_peak = 6773.5
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        with open(pk_path) as f:
+            hbm_peak = float(json.load(f).get("hbm_gbs", hbm_peak))
+    line = {
+        "metric": METRIC, "value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}: B={B},H={H},Nq={Nq},Nk={Nk},d={d},"
+                               f"{'causal' if causal else 'non-causal'} (split-KV path)",
+                   "l2": "inputs larger than L2 (K+V = %.0f MB)" % (2 * k.numel() * 2 / 1e6),
+                   "workspace_bytes": ws_bytes},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": gbs / hbm_peak, "traffic": None,
+                     "algorithmic_bytes_per_step": algo_bytes,
+                     "kernel": f"splitkv_partial_kernel<{d}> + splitkv_merge_kernel<{d}>"},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="cfg5", choices=sorted(synth.CONFIGS))
+    ap.add_argument("--config", default="cfg5",
+                    choices=sorted(synth.CONFIGS) + sorted(synth.DECODE_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
     args = ap.parse_args()
     name = args.config
+    if name in synth.DECODE_CONFIGS:
+        return run_decode(args, name)
     c = synth.CONFIGS[name]
     if args.impl == "reference":
         return run_reference(args, c, name)

@@ -47,6 +47,10 @@ def lib() -> ctypes.CDLL:
         L.mha_set_wait_limit.restype = i
         L.mha_wait_selftest.argtypes = [ctypes.c_longlong, vp]
         L.mha_wait_selftest.restype = i
+        L.mha_fwd_kv.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp, ctypes.c_size_t, vp]
+        L.mha_fwd_kv.restype = i
+        L.mha_fwd_kv_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.mha_fwd_kv_workspace_size.restype = ctypes.c_size_t
         _lib = L
     return _lib
 
@@ -113,4 +117,34 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, stream=No
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     mha_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream)
+    return o, lse
+
+
+def mha_fwd_kv_workspace_size(B: int, H: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    return int(lib().mha_fwd_kv_workspace_size(int(B), int(H), int(Nq), int(Nk), int(d), int(num_splits)))
+
+
+def mha_fwd_kv(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+               causal: bool, num_splits: int, workspace, workspace_bytes: int, stream=None) -> None:
+    """C ``mha_fwd_kv``: tensors (or raw device addresses) in, status checked."""
+    rc = lib().mha_fwd_kv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H), int(Nq),
+                          int(Nk), int(d), ctypes.c_float(scale), int(bool(causal)), int(num_splits),
+                          _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_fwd_kv")
+
+
+def forward_kv(q, k, v, causal: bool = False, scale: float | None = None, num_splits: int = 0,
+               stream=None):
+    """Allocate O, LSE and the workspace with torch and run ``mha_fwd_kv``."""
+    import torch
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if scale is None:
+        scale = float(torch.tensor(d, dtype=torch.float32).rsqrt())
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+    ws_bytes = mha_fwd_kv_workspace_size(B, H, Nq, Nk, d, num_splits)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    mha_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, ws, ws_bytes, stream)
     return o, lse

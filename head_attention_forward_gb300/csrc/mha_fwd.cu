@@ -15,6 +15,7 @@
 
 #include "mha_fwd.h"
 #include "mha_fwd_kernel.cuh"
+#include "mha_internal.h"
 
 namespace {
 
@@ -34,6 +35,10 @@ struct DeviceState {
   unsigned* status = nullptr;
 };
 DeviceState g_dev[kMaxDevices];
+
+}  // namespace
+
+namespace mha_host {
 
 // Per-device set-up, done once under the lock: check the architecture,
 // raise the dynamic shared-memory limit of every kernel instantiation and
@@ -93,14 +98,12 @@ int device_setup(int* dev_out, unsigned** status_out) {
   return MHA_OK;
 }
 
-// 3-D view [BH][N][d] of a contiguous bf16 tensor; box = 64 x 128 x 1 with
-// the 128-byte swizzle the MMA descriptors expect.  Rows past N read as 0.
-bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
+bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -110,6 +113,21 @@ bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+long long wait_limit() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_wait_limit;
+}
+
+}  // namespace mha_host
+
+namespace {
+using namespace mha_host;
 
 template <int D, bool CAUSAL>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
@@ -155,10 +173,6 @@ int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   // the outputs must not overlap the inputs
   const uintptr_t tb = static_cast<uintptr_t>(BH) * N * d * 2;
   const uintptr_t lb = static_cast<uintptr_t>(BH) * N * 4;
-  auto overlap = [](const void* a, uintptr_t na, const void* b, uintptr_t nb) {
-    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-    return x < y + nb && y < x + na;
-  };
   for (const void* in : {q, k, v})
     if (overlap(o, tb, in, tb) || overlap(lse, lb, in, tb)) return MHA_ERR_INVALID_ARG;
   if (overlap(o, tb, lse, lb)) return MHA_ERR_INVALID_ARG;
@@ -169,19 +183,16 @@ int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   if (rc != MHA_OK) return rc;
 
   CUtensorMap mq, mk, mv;
-  if (!encode_map(&mq, q, static_cast<int>(BH), N, d) ||
-      !encode_map(&mk, k, static_cast<int>(BH), N, d) ||
-      !encode_map(&mv, v, static_cast<int>(BH), N, d))
+  if (!encode_map(&mq, q, static_cast<int>(BH), N, d, 128) ||
+      !encode_map(&mk, k, static_cast<int>(BH), N, d, 128) ||
+      !encode_map(&mv, v, static_cast<int>(BH), N, d, 128))
     return MHA_ERR_CUDA;
 
   mha::FwdParams prm;
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.status = status;
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    prm.wait_limit = g_wait_limit;
-  }
+  prm.wait_limit = wait_limit();
   prm.N = N;
   prm.num_mblocks = (N + 255) / 256;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);

@@ -1,0 +1,26 @@
+// mha_internal.h - host-side helpers shared by the library's translation
+// units (not part of the public C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cstddef>
+
+namespace mha_host {
+
+// Once per device: architecture check, driver entry point lookup, status
+// word address.  Returns an mha_status code; on success fills dev / status.
+int device_setup(int* dev, unsigned** status);
+
+// 3-D TMA view [BH][N][d] of a contiguous bf16 tensor, box 64 x box_rows x 1,
+// 128-byte swizzle; rows past N read as zero.
+bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
+
+// Cycle budget of every device-side wait for launches made now.
+long long wait_limit();
+
+bool aligned16(const void* p);
+
+// True when [a, a+na) and [b, b+nb) overlap.
+bool overlap(const void* a, size_t na, const void* b, size_t nb);
+
+}  // namespace mha_host

@@ -1,0 +1,192 @@
+// mha_splitkv.cu - host side of the split-KV attention forward (a few
+// queries against a long key/value sequence): argument checks, workspace
+// layout, split count, TMA maps and the two launches.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+#include <type_traits>
+
+#include "mha_fwd.h"
+#include "mha_internal.h"
+#include "mha_splitkv_kernel.cuh"
+
+namespace {
+
+using namespace mha_host;
+
+constexpr int kMaxDevices = 64;
+// Target CTA count when the caller lets the library pick the split count:
+// four waves of two CTAs per SM on a 152-SM part.  A fixed constant keeps the
+// workspace size a pure function of the problem shape.
+constexpr int kTargetCtas = 4 * 2 * 152;
+
+std::mutex g_mu;
+bool g_attr_done[kMaxDevices] = {};
+
+template <int V>
+using Int = std::integral_constant<int, V>;
+
+// Calls f(Int<D>, Int<QB>) for every compiled partial-kernel variant.
+template <typename F>
+void for_each_variant(F&& f) {
+  f(Int<64>(), Int<1>()); f(Int<64>(), Int<2>()); f(Int<64>(), Int<4>());
+  f(Int<64>(), Int<8>()); f(Int<64>(), Int<16>());
+  f(Int<128>(), Int<1>()); f(Int<128>(), Int<2>()); f(Int<128>(), Int<4>());
+  f(Int<128>(), Int<8>()); f(Int<128>(), Int<16>());
+}
+
+int query_bucket(int Nq) { return Nq <= 1 ? 1 : Nq <= 2 ? 2 : Nq <= 4 ? 4 : Nq <= 8 ? 8 : 16; }
+
+template <int D, int QB>
+cudaError_t launch_partial(cudaLaunchConfig_t cfg, const CUtensorMap& mk, const CUtensorMap& mv,
+                           const mha::SplitParams& prm) {
+  cfg.dynamicSmemBytes = mha::SplitCfg<D, QB>::kSmemBytes;
+  return cudaLaunchKernelEx(&cfg, mha::splitkv_partial_kernel<D, QB>, mk, mv, prm);
+}
+
+template <int D>
+cudaError_t launch_partial_d(cudaLaunchConfig_t cfg, const CUtensorMap& mk, const CUtensorMap& mv,
+                             const mha::SplitParams& prm) {
+  switch (query_bucket(prm.Nq)) {
+    case 1: return launch_partial<D, 1>(cfg, mk, mv, prm);
+    case 2: return launch_partial<D, 2>(cfg, mk, mv, prm);
+    case 4: return launch_partial<D, 4>(cfg, mk, mv, prm);
+    case 8: return launch_partial<D, 8>(cfg, mk, mv, prm);
+    default: return launch_partial<D, 16>(cfg, mk, mv, prm);
+  }
+}
+
+int setup(int* dev, unsigned** status) {
+  const int rc = device_setup(dev, status);
+  if (rc != MHA_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_attr_done[*dev]) {
+    bool fail = false;
+    for_each_variant([&](auto d_tag, auto q_tag) {
+      constexpr int D = decltype(d_tag)::value, QB = decltype(q_tag)::value;
+      fail |= cudaFuncSetAttribute(mha::splitkv_partial_kernel<D, QB>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   mha::SplitCfg<D, QB>::kSmemBytes) != cudaSuccess;
+    });
+    if (fail) return MHA_ERR_CUDA;
+    g_attr_done[*dev] = true;
+  }
+  return MHA_OK;
+}
+
+struct Plan {
+  int splits = 0, tiles_per_split = 0;
+  size_t o_part_bytes = 0, lse_part_bytes = 0, total = 0;
+};
+
+// Split count and workspace layout: o_part fp32 [BH, splits, Nq, d], then
+// (16-byte aligned) lse_part fp32 [BH, splits, Nq].
+Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits) {
+  Plan pl;
+  const int tiles = (Nk + 63) / 64;
+  int want = num_splits > 0 ? num_splits
+                            : static_cast<int>(std::max<long long>(1, (kTargetCtas + BH - 1) / BH));
+  want = std::max(1, std::min(want, tiles));
+  pl.tiles_per_split = (tiles + want - 1) / want;
+  pl.splits = (tiles + pl.tiles_per_split - 1) / pl.tiles_per_split;
+  pl.o_part_bytes = static_cast<size_t>(BH) * pl.splits * Nq * d * 4;
+  pl.lse_part_bytes = static_cast<size_t>(BH) * pl.splits * Nq * 4;
+  pl.total = ((pl.o_part_bytes + 15) & ~static_cast<size_t>(15)) + pl.lse_part_bytes;
+  return pl;
+}
+
+int check_shape(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || num_splits < 0) return MHA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return MHA_ERR_UNSUPPORTED_DIM;
+  if (Nq > mha::kSplitMaxQ) return MHA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * H > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
+  return MHA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t mha_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits) {
+  if (check_shape(B, H, Nq, Nk, d, num_splits) != MHA_OK) return 0;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH == 0 || Nq == 0 || Nk == 0) return 0;
+  return make_plan(BH, Nq, Nk, d, num_splits).total;
+}
+
+int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+               int Nq, int Nk, int d, float scale, int causal, int num_splits, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  int rc = check_shape(B, H, Nq, Nk, d, num_splits);
+  if (rc != MHA_OK) return rc;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return MHA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH == 0 || Nq == 0) return MHA_OK;
+  if (Nk == 0) return MHA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse || !workspace) return MHA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
+      !aligned16(workspace))
+    return MHA_ERR_MISALIGNED;
+  const Plan pl = make_plan(BH, Nq, Nk, d, num_splits);
+  if (workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
+  const size_t qb = static_cast<size_t>(BH) * Nq * d * 2, kb = static_cast<size_t>(BH) * Nk * d * 2;
+  const size_t lb = static_cast<size_t>(BH) * Nq * 4;
+  // outputs and workspace must not overlap the inputs or each other
+  const void* ins[3] = {q, k, v};
+  const size_t in_bytes[3] = {qb, kb, kb};
+  for (int i = 0; i < 3; ++i)
+    if (overlap(o, qb, ins[i], in_bytes[i]) || overlap(lse, lb, ins[i], in_bytes[i]) ||
+        overlap(workspace, pl.total, ins[i], in_bytes[i]))
+      return MHA_ERR_INVALID_ARG;
+  if (overlap(o, qb, lse, lb) || overlap(o, qb, workspace, pl.total) ||
+      overlap(lse, lb, workspace, pl.total))
+    return MHA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  unsigned* status = nullptr;
+  rc = setup(&dev, &status);
+  if (rc != MHA_OK) return rc;
+  CUtensorMap mk, mv;
+  if (!encode_map(&mk, k, static_cast<int>(BH), Nk, d, 64) ||
+      !encode_map(&mv, v, static_cast<int>(BH), Nk, d, 64))
+    return MHA_ERR_CUDA;
+
+  mha::SplitParams prm;
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.o_part = static_cast<float*>(workspace);
+  prm.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          ((pl.o_part_bytes + 15) & ~static_cast<size_t>(15)));
+  prm.status = status;
+  prm.wait_limit = wait_limit();
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.num_splits = pl.splits;
+  prm.tiles_per_split = pl.tiles_per_split;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.causal = causal ? 1 : 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.splits), static_cast<unsigned>(BH), 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = st;
+  cudaError_t err = d == 64 ? launch_partial_d<64>(cfg, mk, mv, prm)
+                            : launch_partial_d<128>(cfg, mk, mv, prm);
+  if (err != cudaSuccess) return MHA_ERR_CUDA;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(static_cast<unsigned>(Nq), static_cast<unsigned>(BH), 1);
+  mcfg.blockDim = dim3(static_cast<unsigned>(d), 1, 1);
+  mcfg.stream = st;
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+  if (d == 64)
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, static_cast<const float*>(prm.o_part),
+                             static_cast<const float*>(prm.lse_part), ob, lse, Nq, pl.splits);
+  else
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, static_cast<const float*>(prm.o_part),
+                             static_cast<const float*>(prm.lse_part), ob, lse, Nq, pl.splits);
+  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -28,6 +28,8 @@
 #ifndef MHA_FWD_H
 #define MHA_FWD_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -64,6 +66,41 @@ typedef enum {
  */
 int mha_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
             int B, int H, int N, int d, float scale, int causal, void *stream);
+
+/*
+ * mha_fwd_kv - attention forward for a few queries against a long key/value
+ * sequence (decode), computed by splitting the keys across CTAs and merging
+ * the partial results by their log-sum-exp ("flash decoding": the split of
+ * keys and values across workers and the reduction of their partial results
+ * that the ML-Triton paper describes in section 3.2).
+ *
+ *   q       : bf16 [B, H, Nq, d], device, read only; 0 <= Nq <= 16.
+ *   k, v    : bf16 [B, H, Nk, d], device, read only; Nk >= 1.
+ *   o       : bf16 [B, H, Nq, d], device, written.
+ *   lse     : fp32 [B, H, Nq], device, written (natural log).
+ *   d       : 64 or 128.  scale: finite and > 0.
+ *   causal  : 0 = every query sees every key; non-zero = the queries are the
+ *             last Nq positions of the sequence (bottom-right alignment):
+ *             query i sees keys 0 .. Nk-Nq+i.  With Nq == Nk this is the
+ *             mask of mha_fwd.  A query with no visible key gets O = 0 and
+ *             LSE = -inf.
+ *   num_splits : number of key splits, or 0 to let the library choose.
+ *   workspace, workspace_bytes : device scratch owned by the caller, 16-byte
+ *             aligned, at least mha_fwd_kv_workspace_size(...) bytes, not
+ *             overlapping any other argument.  Its contents need no
+ *             initialisation and are garbage afterwards.
+ *   stream  : cudaStream_t; two kernels are queued on it.
+ *
+ * B*H == 0 or Nq == 0 is a no-op.  Errors as for mha_fwd.
+ */
+int mha_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
+               int B, int H, int Nq, int Nk, int d, float scale, int causal,
+               int num_splits, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes mha_fwd_kv needs for this shape and split request (0 for
+ * an empty problem or invalid arguments).  A pure function of its arguments;
+ * no CUDA call. */
+size_t mha_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
 
 /* A short, static, human-readable description of a status code. */
 const char *mha_strerror(int status);

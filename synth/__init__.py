@@ -169,3 +169,23 @@ CONFIGS = {
 def config_inputs(name: str, compiled: bool = True):
     c = CONFIGS[name]
     return qkv(c["seed"], c["B"], c["H"], c["N"], c["d"], c["sigma_qk"], c["sigma_v"], compiled)
+
+
+# Decode-shaped workloads for the split-KV path: Nq queries (the newest
+# positions) against Nk cached keys; K and V far larger than the 129 MB L2.
+DECODE_CONFIGS = {
+    "dec1": dict(B=8, H=32, Nq=1, Nk=32768, d=128, causal=False, seed=5),
+    "dec2": dict(B=1, H=32, Nq=4, Nk=131072, d=128, causal=True, seed=6),
+    "dec3": dict(B=16, H=16, Nq=8, Nk=8192, d=64, causal=True, seed=7),
+}
+
+
+def decode_inputs(name: str, compiled: bool = True):
+    """q [B,H,Nq,d], k and v [B,H,Nk,d] as bf16 bit arrays."""
+    c = DECODE_CONFIGS[name]
+    gen = normal_bf16_c if compiled else normal_bf16
+    B, H, Nq, Nk, d = c["B"], c["H"], c["Nq"], c["Nk"], c["d"]
+    q = gen(c["seed"], STREAM_Q, B * H * Nq * d).reshape(B, H, Nq, d)
+    k = gen(c["seed"], STREAM_K, B * H * Nk * d).reshape(B, H, Nk, d)
+    v = gen(c["seed"], STREAM_V, B * H * Nk * d).reshape(B, H, Nk, d)
+    return q, k, v

@@ -88,3 +88,37 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(b, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         b.lib()
+
+
+def test_kv_workspace_size_is_pure():
+    import head_attention_forward_gb300 as mha
+    a = mha.mha_fwd_kv_workspace_size(2, 8, 1, 32768, 128, 0)
+    assert a > 0 and a == mha.mha_fwd_kv_workspace_size(2, 8, 1, 32768, 128, 0)
+    # explicit split count: o_part (fp32) + 16-byte aligned lse_part
+    assert mha.mha_fwd_kv_workspace_size(1, 1, 4, 1000, 64, 2) == 2 * 4 * 64 * 4 + 2 * 4 * 4
+    assert mha.mha_fwd_kv_workspace_size(1, 1, 17, 100, 64, 0) == 0   # Nq > 16
+    assert mha.mha_fwd_kv_workspace_size(1, 1, 1, 100, 96, 0) == 0    # bad d
+    assert mha.mha_fwd_kv_workspace_size(0, 1, 1, 100, 64, 0) == 0    # empty
+
+
+def test_kv_argument_checks(L):
+    import head_attention_forward_gb300 as mha
+    big = 1 << 40
+    args = dict(q=big, k=2 * big, v=3 * big, o=4 * big, lse=5 * big, B=1, H=1, Nq=1, Nk=100,
+                d=64, scale=0.125, causal=0, splits=0, ws=6 * big, wsb=1 << 20)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return L.mha_fwd_kv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"],
+                            a["Nk"], a["d"], ctypes.c_float(a["scale"]), a["causal"], a["splits"],
+                            a["ws"], a["wsb"], None)
+    assert call(d=96) == mha.MHA_ERR_UNSUPPORTED_DIM
+    assert call(Nq=17) == mha.MHA_ERR_INVALID_ARG
+    assert call(Nk=0) == mha.MHA_ERR_INVALID_ARG
+    assert call(splits=-1) == mha.MHA_ERR_INVALID_ARG
+    assert call(ws=0) == mha.MHA_ERR_INVALID_ARG
+    assert call(wsb=16) == mha.MHA_ERR_INVALID_ARG            # workspace too small
+    assert call(ws=6 * big + 4) == mha.MHA_ERR_MISALIGNED
+    assert call(ws=2 * big) == mha.MHA_ERR_INVALID_ARG        # workspace over k
+    assert call(scale=-1.0) == mha.MHA_ERR_INVALID_ARG
+    assert call(Nq=0) == mha.MHA_OK and call(B=0) == mha.MHA_OK

@@ -18,6 +18,7 @@ MHA_ERR_MISALIGNED = 3
 MHA_ERR_CUDA = 4
 MHA_ERR_TIMEOUT = 5
 MHA_ERR_NO_DEVICE = 6
+MHA_ERR_SCRATCH_LIMIT = 7
 
 _lib = None
 
@@ -51,6 +52,8 @@ def lib() -> ctypes.CDLL:
         L.mha_fwd_kv.restype = i
         L.mha_fwd_kv_workspace_size.argtypes = [i, i, i, i, i, i]
         L.mha_fwd_kv_workspace_size.restype = ctypes.c_size_t
+        L.mha_fwd_kv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
+        L.mha_fwd_kv_noalloc.restype = i
         _lib = L
     return _lib
 
@@ -148,3 +151,14 @@ def forward_kv(q, k, v, causal: bool = False, scale: float | None = None, num_sp
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
     mha_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, ws, ws_bytes, stream)
     return o, lse
+
+
+def mha_fwd_kv_noalloc(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int, scale: float,
+                       causal: bool, num_splits: int = 0, stream=None) -> None:
+    """C ``mha_fwd_kv_noalloc``: the split-KV forward on the library's built-in
+    scratch buffer, for callers that cannot allocate device memory."""
+    rc = lib().mha_fwd_kv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(H),
+                                  int(Nq), int(Nk), int(d), ctypes.c_float(scale), int(bool(causal)),
+                                  int(num_splits), _stream(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_fwd_kv_noalloc")

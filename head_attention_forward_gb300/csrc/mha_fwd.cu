@@ -155,6 +155,7 @@ const char* mha_strerror(int status) {
     case MHA_ERR_CUDA: return "CUDA call failed";
     case MHA_ERR_TIMEOUT: return "device-side wait timed out";
     case MHA_ERR_NO_DEVICE: return "no usable sm_103 device";
+    case MHA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the built-in 16 MiB buffer";
     default: return "unknown status";
   }
 }

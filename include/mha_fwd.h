@@ -42,7 +42,9 @@ typedef enum {
     MHA_ERR_MISALIGNED = 3,      /* a pointer is not 16-byte aligned          */
     MHA_ERR_CUDA = 4,            /* a CUDA runtime or driver call failed      */
     MHA_ERR_TIMEOUT = 5,         /* a device-side wait ran past its limit     */
-    MHA_ERR_NO_DEVICE = 6        /* no usable sm_103 device is current        */
+    MHA_ERR_NO_DEVICE = 6,       /* no usable sm_103 device is current        */
+    MHA_ERR_SCRATCH_LIMIT = 7    /* mha_fwd_kv_noalloc: the problem needs more
+                                    scratch than the built-in buffer holds   */
 } mha_status;
 
 /*
@@ -101,6 +103,36 @@ int mha_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
  * an empty problem or invalid arguments).  A pure function of its arguments;
  * no CUDA call. */
 size_t mha_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_splits);
+
+/*
+ * mha_fwd_kv_noalloc - mha_fwd_kv for callers that cannot allocate device
+ * memory.  (The pages this library follows have no counterpart: this entry
+ * point exists for deployment reasons only.)
+ *
+ * Some callers hold raw device pointers to their inputs and outputs but
+ * cannot obtain a workspace: a plug-in inside another runtime that owns all
+ * allocations, a service that reserves its memory at start-up and may not
+ * allocate while serving, a host program with no access to the allocator
+ * behind its buffers.  This call takes the same arguments as mha_fwd_kv
+ * minus the workspace and uses a scratch buffer of 16 MiB (16777216 bytes)
+ * that the library keeps in its own module memory on every GPU that loads
+ * it, for the life of the process.  It allocates nothing.
+ *
+ *   - Problems whose workspace (mha_fwd_kv_workspace_size with the same
+ *     arguments) exceeds 16 MiB are rejected with MHA_ERR_SCRATCH_LIMIT
+ *     before any CUDA call; other argument errors as for mha_fwd_kv.
+ *   - The first call on each device looks up the buffer's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture begins.
+ *   - All calls on a device share the one buffer, and it keeps whatever the
+ *     last call left there.  Nothing in it needs to start at zero: every
+ *     element a call reads back was written earlier in the same call.  Calls
+ *     whose execution overlaps on the GPU (for example on two streams) race
+ *     on the buffer and must be serialised by the caller.
+ */
+int mha_fwd_kv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int H, int Nq, int Nk, int d, float scale, int causal,
+                       int num_splits, void *stream);
 
 /* A short, static, human-readable description of a status code. */
 const char *mha_strerror(int status);

@@ -311,13 +311,86 @@ def run_decode(args, name):
     return 0
 
 
+def hbm_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f).get("hbm_gbs", 6773.5)), "measured (MEASURED_PEAKS.json hbm_gbs)"
+    return 6800.0, "fallback (no MEASURED_PEAKS.json)"
+
+
+def run_paged(args, name):
+    """Paged-KV path on a decode workload with mixed sequence lengths."""
+    import torch
+
+    import head_attention_forward_gb300 as mha
+    c = synth.PAGED_CONFIGS[name]
+    B, H, Nq, d, page, causal = c["B"], c["H"], c["Nq"], c["d"], c["page"], c["causal"]
+    qb, kcb, vcb, table, seq = synth.paged_inputs(name)
+    num_blocks, max_blocks = kcb.shape[0], table.shape[1]
+    torch.cuda.set_device(0)
+    mha.build()
+    mha.lib()
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, kc, vc = dev(qb), dev(kcb), dev(vcb)
+    td, sd = torch.from_numpy(table).cuda(), torch.from_numpy(seq).cuda()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, max_blocks * page, d, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    stream = torch.cuda.current_stream()
+    sptr = int(stream.cuda_stream)
+
+    def step():
+        mha.mha_fwd_paged(q, kc, vc, td, sd, o, lse, B, H, Nq, d, page, num_blocks, max_blocks, scale,
+                          causal, 0, ws, ws_bytes, sptr)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(0) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    rc, word = mha.mha_device_status(sptr)
+    if rc != mha.MHA_OK:
+        raise RuntimeError(f"device status {rc} ({word:#x})")
+    ms = e0.elapsed_time(e1) / args.steps
+    keys = int(seq.astype(np.int64).sum())
+    flops = 4.0 * H * Nq * keys * d
+    algo_bytes = 2 * 2 * keys * H * d + 2 * (q.numel() + o.numel()) + 4 * lse.numel() + table.nbytes + seq.nbytes
+    gbs = algo_bytes / (ms / 1e3) / 1e9
+    peak, src = hbm_peak_gbs()
+    print(json.dumps({
+        "metric": METRIC, "value": flops / (ms / 1e3) / 1e12, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name}: B={B},H={H},Nq={Nq},d={d},page={page},"
+                               f"seq {int(seq.min())}..{int(seq.max())} (paged-KV path)",
+                   "cached_keys": keys, "l2": "K/V caches larger than L2 (%.0f MB)" % (2 * kc.numel() * 2 / 1e6)},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_source": src, "traffic": None, "algorithmic_bytes_per_step": algo_bytes,
+                     "kernel": f"splitkv_partial_kernel<{d},paged> + splitkv_merge_kernel<{d}>"},
+        "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+    }), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="cfg5",
-                    choices=sorted(synth.CONFIGS) + sorted(synth.DECODE_CONFIGS))
+                    choices=sorted(synth.CONFIGS) + sorted(synth.DECODE_CONFIGS)
+                    + sorted(synth.PAGED_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -325,6 +398,8 @@ def main():
     name = args.config
     if name in synth.DECODE_CONFIGS:
         return run_decode(args, name)
+    if name in synth.PAGED_CONFIGS:
+        return run_paged(args, name)
     c = synth.CONFIGS[name]
     if args.impl == "reference":
         return run_reference(args, c, name)

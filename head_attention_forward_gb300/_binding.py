@@ -52,6 +52,9 @@ def lib() -> ctypes.CDLL:
         L.mha_fwd_kv.restype = i
         L.mha_fwd_kv_workspace_size.argtypes = [i, i, i, i, i, i]
         L.mha_fwd_kv_workspace_size.restype = ctypes.c_size_t
+        L.mha_fwd_paged.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, i, f, i, i, vp,
+                                    ctypes.c_size_t, vp]
+        L.mha_fwd_paged.restype = i
         L.mha_fwd_kv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
         L.mha_fwd_kv_noalloc.restype = i
         _lib = L
@@ -162,3 +165,16 @@ def mha_fwd_kv_noalloc(q, k, v, o, lse, B: int, H: int, Nq: int, Nk: int, d: int
                                   int(num_splits), _stream(stream))
     if rc != MHA_OK:
         raise MhaError(rc, "mha_fwd_kv_noalloc")
+
+
+def mha_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B: int, H: int, Nq: int,
+                  d: int, page_size: int, num_blocks: int, max_blocks: int, scale: float,
+                  causal: bool, num_splits: int, workspace, workspace_bytes: int, stream=None) -> None:
+    """C ``mha_fwd_paged``: tensors (or raw device addresses) in, status checked."""
+    rc = lib().mha_fwd_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+                             _ptr(o), _ptr(lse), int(B), int(H), int(Nq), int(d), int(page_size),
+                             int(num_blocks), int(max_blocks), ctypes.c_float(scale),
+                             int(bool(causal)), int(num_splits), _ptr(workspace), int(workspace_bytes),
+                             _stream(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_fwd_paged")

@@ -112,6 +112,22 @@ bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int bo
   return r == CUDA_SUCCESS;
 }
 
+bool encode_paged_map(CUtensorMap* map, const void* base, int num_blocks, int H, int page_size,
+                      int d) {
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(page_size),
+                        static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(num_blocks)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(page_size) * d * 2,
+                           static_cast<cuuint64_t>(H) * page_size * d * 2};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(page_size < 64 ? page_size : 64), 1, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlap(const void* a, size_t na, const void* b, size_t nb) {

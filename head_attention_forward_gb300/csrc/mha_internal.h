@@ -15,6 +15,11 @@ int device_setup(int* dev, unsigned** status);
 // 128-byte swizzle; rows past N read as zero.
 bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);
 
+// 4-D TMA view [num_blocks][H][page_size][d] of a paged bf16 K or V cache,
+// box 64 x min(page_size, 64) x 1 x 1, 128-byte swizzle; out-of-range block
+// ids read as zero.
+bool encode_paged_map(CUtensorMap* map, const void* base, int num_blocks, int H, int page_size, int d);
+
 // Cycle budget of every device-side wait for launches made now.
 long long wait_limit();
 

@@ -25,57 +25,6 @@ constexpr int kTargetCtas = 4 * 2 * 152;
 std::mutex g_mu;
 bool g_attr_done[kMaxDevices] = {};
 
-template <int V>
-using Int = std::integral_constant<int, V>;
-
-// Calls f(Int<D>, Int<QB>) for every compiled partial-kernel variant.
-template <typename F>
-void for_each_variant(F&& f) {
-  f(Int<64>(), Int<1>()); f(Int<64>(), Int<2>()); f(Int<64>(), Int<4>());
-  f(Int<64>(), Int<8>()); f(Int<64>(), Int<16>());
-  f(Int<128>(), Int<1>()); f(Int<128>(), Int<2>()); f(Int<128>(), Int<4>());
-  f(Int<128>(), Int<8>()); f(Int<128>(), Int<16>());
-}
-
-int query_bucket(int Nq) { return Nq <= 1 ? 1 : Nq <= 2 ? 2 : Nq <= 4 ? 4 : Nq <= 8 ? 8 : 16; }
-
-template <int D, int QB>
-cudaError_t launch_partial(cudaLaunchConfig_t cfg, const CUtensorMap& mk, const CUtensorMap& mv,
-                           const mha::SplitParams& prm) {
-  cfg.dynamicSmemBytes = mha::SplitCfg<D, QB>::kSmemBytes;
-  return cudaLaunchKernelEx(&cfg, mha::splitkv_partial_kernel<D, QB>, mk, mv, prm);
-}
-
-template <int D>
-cudaError_t launch_partial_d(cudaLaunchConfig_t cfg, const CUtensorMap& mk, const CUtensorMap& mv,
-                             const mha::SplitParams& prm) {
-  switch (query_bucket(prm.Nq)) {
-    case 1: return launch_partial<D, 1>(cfg, mk, mv, prm);
-    case 2: return launch_partial<D, 2>(cfg, mk, mv, prm);
-    case 4: return launch_partial<D, 4>(cfg, mk, mv, prm);
-    case 8: return launch_partial<D, 8>(cfg, mk, mv, prm);
-    default: return launch_partial<D, 16>(cfg, mk, mv, prm);
-  }
-}
-
-int setup(int* dev, unsigned** status) {
-  const int rc = device_setup(dev, status);
-  if (rc != MHA_OK) return rc;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_attr_done[*dev]) {
-    bool fail = false;
-    for_each_variant([&](auto d_tag, auto q_tag) {
-      constexpr int D = decltype(d_tag)::value, QB = decltype(q_tag)::value;
-      fail |= cudaFuncSetAttribute(mha::splitkv_partial_kernel<D, QB>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   mha::SplitCfg<D, QB>::kSmemBytes) != cudaSuccess;
-    });
-    if (fail) return MHA_ERR_CUDA;
-    g_attr_done[*dev] = true;
-  }
-  return MHA_OK;
-}
-
 struct Plan {
   int splits = 0, tiles_per_split = 0;
   size_t o_part_bytes = 0, lse_part_bytes = 0, total = 0;
@@ -102,6 +51,86 @@ int check_shape(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (d != 64 && d != 128) return MHA_ERR_UNSUPPORTED_DIM;
   if (Nq > mha::kSplitMaxQ) return MHA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
+  return MHA_OK;
+}
+
+template <int V>
+using Int = std::integral_constant<int, V>;
+
+// Calls f(Int<D>, Int<QB>) for every compiled partial-kernel variant.
+template <typename F>
+void for_each_variant(F&& f) {
+  f(Int<64>(), Int<1>()); f(Int<64>(), Int<2>()); f(Int<64>(), Int<4>());
+  f(Int<64>(), Int<8>()); f(Int<64>(), Int<16>());
+  f(Int<128>(), Int<1>()); f(Int<128>(), Int<2>()); f(Int<128>(), Int<4>());
+  f(Int<128>(), Int<8>()); f(Int<128>(), Int<16>());
+}
+
+int query_bucket(int Nq) { return Nq <= 1 ? 1 : Nq <= 2 ? 2 : Nq <= 4 ? 4 : Nq <= 8 ? 8 : 16; }
+
+template <int D, int QB, bool PAGED>
+cudaError_t launch_partial(cudaLaunchConfig_t cfg, const CUtensorMap& mk, const CUtensorMap& mv,
+                           const mha::SplitParams& prm) {
+  cfg.dynamicSmemBytes = mha::SplitCfg<D, QB>::kSmemBytes;
+  return cudaLaunchKernelEx(&cfg, mha::splitkv_partial_kernel<D, QB, PAGED>, mk, mv, prm);
+}
+
+template <int D, bool PAGED>
+cudaError_t launch_partial_d(cudaLaunchConfig_t cfg, const CUtensorMap& mk, const CUtensorMap& mv,
+                             const mha::SplitParams& prm) {
+  switch (query_bucket(prm.Nq)) {
+    case 1: return launch_partial<D, 1, PAGED>(cfg, mk, mv, prm);
+    case 2: return launch_partial<D, 2, PAGED>(cfg, mk, mv, prm);
+    case 4: return launch_partial<D, 4, PAGED>(cfg, mk, mv, prm);
+    case 8: return launch_partial<D, 8, PAGED>(cfg, mk, mv, prm);
+    default: return launch_partial<D, 16, PAGED>(cfg, mk, mv, prm);
+  }
+}
+
+// Partial kernel + merge kernel on `stream` (shared by the contiguous and
+// the paged entry points).
+template <bool PAGED>
+int run_split(const CUtensorMap& mk, const CUtensorMap& mv, mha::SplitParams prm, long long BH,
+              int d, const Plan& pl, void* o, float* lse, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.splits), static_cast<unsigned>(BH), 1);
+  cfg.blockDim = dim3(128, 1, 1);
+  cfg.stream = st;
+  cudaError_t err = d == 64 ? launch_partial_d<64, PAGED>(cfg, mk, mv, prm)
+                            : launch_partial_d<128, PAGED>(cfg, mk, mv, prm);
+  if (err != cudaSuccess) return MHA_ERR_CUDA;
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(static_cast<unsigned>(prm.Nq), static_cast<unsigned>(BH), 1);
+  mcfg.blockDim = dim3(static_cast<unsigned>(d), 1, 1);
+  mcfg.stream = st;
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+  if (d == 64)
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, static_cast<const float*>(prm.o_part),
+                             static_cast<const float*>(prm.lse_part), ob, lse, prm.Nq, pl.splits);
+  else
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, static_cast<const float*>(prm.o_part),
+                             static_cast<const float*>(prm.lse_part), ob, lse, prm.Nq, pl.splits);
+  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+int setup(int* dev, unsigned** status) {
+  const int rc = device_setup(dev, status);
+  if (rc != MHA_OK) return rc;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_attr_done[*dev]) {
+    bool fail = false;
+    for_each_variant([&](auto d_tag, auto q_tag) {
+      constexpr int D = decltype(d_tag)::value, QB = decltype(q_tag)::value;
+      fail |= cudaFuncSetAttribute(mha::splitkv_partial_kernel<D, QB, false>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   mha::SplitCfg<D, QB>::kSmemBytes) != cudaSuccess;
+      fail |= cudaFuncSetAttribute(mha::splitkv_partial_kernel<D, QB, true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   mha::SplitCfg<D, QB>::kSmemBytes) != cudaSuccess;
+    });
+    if (fail) return MHA_ERR_CUDA;
+    g_attr_done[*dev] = true;
+  }
   return MHA_OK;
 }
 
@@ -153,7 +182,7 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
       !encode_map(&mv, v, static_cast<int>(BH), Nk, d, 64))
     return MHA_ERR_CUDA;
 
-  mha::SplitParams prm;
+  mha::SplitParams prm = {};
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.o_part = static_cast<float*>(workspace);
   prm.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
@@ -166,27 +195,72 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
   prm.tiles_per_split = pl.tiles_per_split;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.causal = causal ? 1 : 0;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return run_split<false>(mk, mv, prm, BH, d, pl, o, lse, static_cast<cudaStream_t>(stream));
+}
 
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(pl.splits), static_cast<unsigned>(BH), 1);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.stream = st;
-  cudaError_t err = d == 64 ? launch_partial_d<64>(cfg, mk, mv, prm)
-                            : launch_partial_d<128>(cfg, mk, mv, prm);
-  if (err != cudaSuccess) return MHA_ERR_CUDA;
-  cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(static_cast<unsigned>(Nq), static_cast<unsigned>(BH), 1);
-  mcfg.blockDim = dim3(static_cast<unsigned>(d), 1, 1);
-  mcfg.stream = st;
-  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
-  if (d == 64)
-    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, static_cast<const float*>(prm.o_part),
-                             static_cast<const float*>(prm.lse_part), ob, lse, Nq, pl.splits);
-  else
-    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, static_cast<const float*>(prm.o_part),
-                             static_cast<const float*>(prm.lse_part), ob, lse, Nq, pl.splits);
-  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
+                  const int* seq_lens, void* o, float* lse, int B, int H, int Nq, int d,
+                  int page_size, int num_blocks, int max_blocks, float scale, int causal,
+                  int num_splits, void* workspace, size_t workspace_bytes, void* stream) {
+  if (max_blocks < 0 || num_blocks < 0 || page_size <= 0) return MHA_ERR_INVALID_ARG;
+  if (page_size < 16 || page_size > 256 || (page_size & (page_size - 1)) != 0) return MHA_ERR_INVALID_ARG;
+  const long long max_keys = static_cast<long long>(max_blocks) * page_size;
+  if (max_keys > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
+  int rc = check_shape(B, H, Nq, static_cast<int>(max_keys), d, num_splits);
+  if (rc != MHA_OK) return rc;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return MHA_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH == 0 || Nq == 0) return MHA_OK;
+  if (max_blocks == 0 || num_blocks == 0) return MHA_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse || !workspace)
+    return MHA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||
+      !aligned16(lse) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3))
+    return MHA_ERR_MISALIGNED;
+  const Plan pl = make_plan(BH, Nq, static_cast<int>(max_keys), d, num_splits);
+  if (workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
+  const size_t qb = static_cast<size_t>(BH) * Nq * d * 2;
+  const size_t cb = static_cast<size_t>(num_blocks) * H * page_size * d * 2;
+  const size_t lb = static_cast<size_t>(BH) * Nq * 4;
+  const size_t tb = static_cast<size_t>(B) * max_blocks * 4, sb = static_cast<size_t>(B) * 4;
+  const void* ins[5] = {q, k_cache, v_cache, block_table, seq_lens};
+  const size_t in_bytes[5] = {qb, cb, cb, tb, sb};
+  for (int i = 0; i < 5; ++i)
+    if (overlap(o, qb, ins[i], in_bytes[i]) || overlap(lse, lb, ins[i], in_bytes[i]) ||
+        overlap(workspace, pl.total, ins[i], in_bytes[i]))
+      return MHA_ERR_INVALID_ARG;
+  if (overlap(o, qb, lse, lb) || overlap(o, qb, workspace, pl.total) ||
+      overlap(lse, lb, workspace, pl.total))
+    return MHA_ERR_INVALID_ARG;
+
+  int dev = 0;
+  unsigned* status = nullptr;
+  rc = setup(&dev, &status);
+  if (rc != MHA_OK) return rc;
+  CUtensorMap mk, mv;
+  if (!encode_paged_map(&mk, k_cache, num_blocks, H, page_size, d) ||
+      !encode_paged_map(&mv, v_cache, num_blocks, H, page_size, d))
+    return MHA_ERR_CUDA;
+  mha::SplitParams prm = {};
+  prm.q = static_cast<const __nv_bfloat16*>(q);
+  prm.block_table = block_table;
+  prm.seq_lens = seq_lens;
+  prm.page_size = page_size;
+  prm.max_blocks = max_blocks;
+  prm.num_heads = H;
+  prm.o_part = static_cast<float*>(workspace);
+  prm.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          ((pl.o_part_bytes + 15) & ~static_cast<size_t>(15)));
+  prm.status = status;
+  prm.wait_limit = wait_limit();
+  prm.Nq = Nq;
+  prm.Nk = static_cast<int>(max_keys);
+  prm.num_splits = pl.splits;
+  prm.tiles_per_split = pl.tiles_per_split;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.causal = causal ? 1 : 0;
+  return run_split<true>(mk, mv, prm, BH, d, pl, o, lse, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -30,6 +30,12 @@ constexpr int kSplitMaxQ = 16;  // queries per call (decode-sized blocks)
 
 struct SplitParams {
   const __nv_bfloat16* q;  // [BH, Nq, D]
+  // paged K/V cache (used when the kernel is instantiated with PAGED):
+  // logical key position t of batch entry b lives in physical block
+  // block_table[b * max_blocks + t / page_size], row t % page_size
+  const int* block_table;  // [B, max_blocks]
+  const int* seq_lens;     // [B] keys cached per batch entry
+  int page_size, max_blocks, num_heads;
   float* o_part;           // [BH, splits, Nq, D]  (normalised by the split's own sum)
   float* lse_part;         // [BH, splits, Nq]     (natural log; -inf when empty)
   unsigned* status;        // device status word
@@ -65,6 +71,16 @@ struct SplitCfg {
   static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
 
+// 4-D TMA load (paged cache: x = d, y = row in page, z = head, w = block).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+
 // Byte offset of element (row, col) of a [rows x 64] bf16 box written by TMA
 // with the 128-byte swizzle: 16-byte chunk index XOR (row mod 8).
 __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
@@ -72,7 +88,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int col) {
   return static_cast<uint32_t>(row * 128 + (((chunk ^ (row & 7)) << 4) | ((col & 7) << 1)));
 }
 
-template <int D, int QB>
+template <int D, int QB, bool PAGED>
 __global__ void __launch_bounds__(SplitCfg<D, QB>::kThreads, 2)
     splitkv_partial_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                            const SplitParams p) {
@@ -83,7 +99,10 @@ __global__ void __launch_bounds__(SplitCfg<D, QB>::kThreads, 2)
   const uint32_t sbase = ptx::smem_u32(smem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int split = blockIdx.x, bh = blockIdx.y;
-  const int Nq = p.Nq, Nk = p.Nk;
+  const int Nq = p.Nq;
+  // keys of this (batch, head): fixed, or this batch entry's cached length
+  // (clamped to what its block table row can address)
+  const int Nk = PAGED ? min(p.seq_lens[bh / p.num_heads], p.max_blocks * p.page_size) : p.Nk;
   const int n_tiles_total = (Nk + C::kTileKeys - 1) / C::kTileKeys;
   const int t_begin = split * p.tiles_per_split;
   const int t_end = min(n_tiles_total, t_begin + p.tiles_per_split);
@@ -104,9 +123,27 @@ __global__ void __launch_bounds__(SplitCfg<D, QB>::kThreads, 2)
     const int slot = t % C::kStages;
     ptx::mbar_arrive_expect_tx(full(slot), 2 * C::kTileBytes);
     const int y = (t_begin + t) * C::kTileKeys;
-    for (int h = 0; h < D / 64; ++h) {
-      ptx::tma_load_3d(k_tile(slot) + h * C::kHalfBytes, &tmK, full(slot), h * 64, y, bh);
-      ptx::tma_load_3d(v_tile(slot) + h * C::kHalfBytes, &tmV, full(slot), h * 64, y, bh);
+    if constexpr (PAGED) {
+      // the tile's 64 keys come from one page (pages >= 64 keys) or from
+      // 64 / page_size consecutive pages; each box lands 1024-byte aligned,
+      // so the 128-byte swizzle of the whole tile stays as one box's
+      const int rows = min(p.page_size, C::kTileKeys);
+      const int b = bh / p.num_heads, head = bh % p.num_heads;
+      for (int r0 = 0; r0 < C::kTileKeys; r0 += rows) {
+        const int pos = y + r0;
+        const int page = min(pos / p.page_size, p.max_blocks - 1);
+        const int blk = p.block_table[static_cast<size_t>(b) * p.max_blocks + page];
+        const int row = pos % p.page_size;
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_4d(k_tile(slot) + h * C::kHalfBytes + r0 * 128, &tmK, full(slot), h * 64, row, head, blk);
+          tma_load_4d(v_tile(slot) + h * C::kHalfBytes + r0 * 128, &tmV, full(slot), h * 64, row, head, blk);
+        }
+      }
+    } else {
+      for (int h = 0; h < D / 64; ++h) {
+        ptx::tma_load_3d(k_tile(slot) + h * C::kHalfBytes, &tmK, full(slot), h * 64, y, bh);
+        ptx::tma_load_3d(v_tile(slot) + h * C::kHalfBytes, &tmV, full(slot), h * 64, y, bh);
+      }
     }
   };
 

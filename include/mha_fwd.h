@@ -99,6 +99,37 @@ int mha_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
                int B, int H, int Nq, int Nk, int d, float scale, int causal,
                int num_splits, void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * mha_fwd_paged - mha_fwd_kv over a paged K/V cache: the cache is split into
+ * fixed-size blocks of page_size keys, and each sequence reaches its keys
+ * through a block table (the paged-attention layout the ML-Triton paper
+ * evaluates in sections 3.2 and 4.3).
+ *
+ *   q           : bf16 [B, H, Nq, d], device; 0 <= Nq <= 16.
+ *   k_cache,
+ *   v_cache     : bf16 [num_blocks, H, page_size, d], device.
+ *   block_table : int32 [B, max_blocks], device: logical page i of batch
+ *                 entry b is physical block block_table[b*max_blocks + i].
+ *                 An id outside [0, num_blocks) reads as zeros.
+ *   seq_lens    : int32 [B], device: keys cached for each batch entry
+ *                 (clamped to max_blocks*page_size); key t of entry b is row
+ *                 t % page_size of block block_table[b][t / page_size].
+ *   o, lse      : as for mha_fwd_kv.
+ *   page_size   : 16, 32, 64, 128 or 256.
+ *   causal      : bottom-right aligned per batch entry (query i of entry b
+ *                 sees keys 0 .. seq_lens[b]-Nq+i); a query with no visible
+ *                 key gets O = 0, LSE = -inf.
+ *   workspace   : at least mha_fwd_kv_workspace_size(B, H, Nq,
+ *                 max_blocks*page_size, d, num_splits) bytes.
+ * block_table and seq_lens must be 4-byte aligned; every other pointer
+ * 16-byte aligned.  Other conventions and errors as for mha_fwd_kv.
+ */
+int mha_fwd_paged(const void *q, const void *k_cache, const void *v_cache,
+                  const int *block_table, const int *seq_lens, void *o, float *lse,
+                  int B, int H, int Nq, int d, int page_size, int num_blocks,
+                  int max_blocks, float scale, int causal, int num_splits,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
 /* Workspace bytes mha_fwd_kv needs for this shape and split request (0 for
  * an empty problem or invalid arguments).  A pure function of its arguments;
  * no CUDA call. */

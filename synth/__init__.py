@@ -189,3 +189,35 @@ def decode_inputs(name: str, compiled: bool = True):
     k = gen(c["seed"], STREAM_K, B * H * Nk * d).reshape(B, H, Nk, d)
     v = gen(c["seed"], STREAM_V, B * H * Nk * d).reshape(B, H, Nk, d)
     return q, k, v
+
+
+# Paged-cache decode workloads: B sequences whose lengths spread between
+# lo and hi keys, pages of `page` keys scattered over the cache.
+PAGED_CONFIGS = {
+    "pag1": dict(B=32, H=32, Nq=1, d=128, page=16, lo=2048, hi=16384, causal=False, seed=8),
+    "pag2": dict(B=32, H=32, Nq=1, d=128, page=64, lo=2048, hi=16384, causal=False, seed=9),
+}
+
+
+def paged_inputs(name: str):
+    """q [B,H,Nq,d], k/v caches [num_blocks,H,page,d] (bf16 bits), block table
+    [B, max_blocks] int32 (pages shuffled over the cache) and seq_lens [B]."""
+    c = PAGED_CONFIGS[name]
+    B, H, Nq, d, page = c["B"], c["H"], c["Nq"], c["d"], c["page"]
+    w = words(c["seed"], 3, 0, B)  # stream 3: sequence lengths and page placement
+    span = c["hi"] - c["lo"] + 1
+    seq = (c["lo"] + (w % np.uint64(span)).astype(np.int64)).astype(np.int32)
+    pages = (seq.astype(np.int64) + page - 1) // page
+    max_blocks = int(pages.max())
+    num_blocks = int(pages.sum())
+    order = np.argsort(words(c["seed"], 4, 0, num_blocks), kind="stable").astype(np.int32)
+    table = np.full((B, max_blocks), -1, dtype=np.int32)
+    pos = 0
+    for b in range(B):
+        table[b, :pages[b]] = order[pos:pos + pages[b]]
+        pos += int(pages[b])
+    gen = normal_bf16_c
+    q = gen(c["seed"], STREAM_Q, B * H * Nq * d).reshape(B, H, Nq, d)
+    kc = gen(c["seed"], STREAM_K, num_blocks * H * page * d).reshape(num_blocks, H, page, d)
+    vc = gen(c["seed"], STREAM_V, num_blocks * H * page * d).reshape(num_blocks, H, page, d)
+    return q, kc, vc, table, seq

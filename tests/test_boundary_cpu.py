@@ -122,3 +122,28 @@ def test_kv_argument_checks(L):
     assert call(ws=2 * big) == mha.MHA_ERR_INVALID_ARG        # workspace over k
     assert call(scale=-1.0) == mha.MHA_ERR_INVALID_ARG
     assert call(Nq=0) == mha.MHA_OK and call(B=0) == mha.MHA_OK
+
+
+def test_paged_argument_checks(L):
+    import head_attention_forward_gb300 as mha
+    big = 1 << 40
+    a = dict(q=big, kc=2 * big, vc=3 * big, bt=4 * big, sl=5 * big, o=6 * big, lse=7 * big, B=1,
+             H=1, Nq=1, d=64, page=64, nb=10, mb=4, scale=0.125, causal=0, splits=0, ws=8 * big,
+             wsb=1 << 20)
+
+    def call(**kw):
+        x = dict(a, **kw)
+        return L.mha_fwd_paged(x["q"], x["kc"], x["vc"], x["bt"], x["sl"], x["o"], x["lse"], x["B"],
+                               x["H"], x["Nq"], x["d"], x["page"], x["nb"], x["mb"],
+                               ctypes.c_float(x["scale"]), x["causal"], x["splits"], x["ws"], x["wsb"],
+                               None)
+    assert call(page=48) == mha.MHA_ERR_INVALID_ARG
+    assert call(page=8) == mha.MHA_ERR_INVALID_ARG
+    assert call(page=512) == mha.MHA_ERR_INVALID_ARG
+    assert call(mb=0) == mha.MHA_ERR_INVALID_ARG
+    assert call(nb=0) == mha.MHA_ERR_INVALID_ARG
+    assert call(bt=0) == mha.MHA_ERR_INVALID_ARG
+    assert call(bt=4 * big + 2) == mha.MHA_ERR_MISALIGNED
+    assert call(d=80) == mha.MHA_ERR_UNSUPPORTED_DIM
+    assert call(wsb=8) == mha.MHA_ERR_INVALID_ARG
+    assert call(Nq=0) == mha.MHA_OK

@@ -76,26 +76,37 @@ def load_peaks():
     return FALLBACK_PEAK_SUSTAINED, FALLBACK_PEAK_TFLOPS, "fallback (no MEASURED_PEAKS.json)"
 
 
-def kernel_source_hash() -> str:
+# Source files each kernel is compiled from; a recorded ncu traffic figure is
+# valid only while these are unchanged.
+KERNEL_SOURCES = {
+    "mha_fwd_kernel": ("mha_fwd_kernel.cuh", "sm103_ptx.cuh", "mha_wait.cuh"),
+    "splitkv_partial_kernel": ("mha_splitkv_kernel.cuh", "sm103_ptx.cuh", "mha_wait.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "head_attention_forward_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    for fn in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic(name):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source; otherwise None."""
+    """DRAM bytes per launch of the workload's dominant kernel from the
+    committed ncu summary, if it was taken on that kernel's current source;
+    otherwise None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         rec = json.load(f)
     ent = rec.get(name)
-    if not ent or ent.get("kernel_source_hash") != kernel_source_hash():
+    if not ent or ent.get("kernel_family") not in KERNEL_SOURCES:
+        return None
+    if ent.get("kernel_source_hash") != kernel_source_hash(ent["kernel_family"]):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -301,7 +312,7 @@ def run_decode(args, name):
                    "l2": "inputs larger than L2 (K+V = %.0f MB)" % (2 * k.numel() * 2 / 1e6),
                    "workspace_bytes": ws_bytes},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": gbs / hbm_peak, "traffic": None,
+                     "frac": gbs / hbm_peak, "traffic": recorded_traffic(name),
                      "algorithmic_bytes_per_step": algo_bytes,
                      "kernel": f"splitkv_partial_kernel<{d}> + splitkv_merge_kernel<{d}>"},
         "gpu_launches": 2 * args.steps,
@@ -376,7 +387,8 @@ def run_paged(args, name):
                                f"seq {int(seq.min())}..{int(seq.max())} (paged-KV path)",
                    "cached_keys": keys, "l2": "K/V caches larger than L2 (%.0f MB)" % (2 * kc.numel() * 2 / 1e6)},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
-                     "peak_source": src, "traffic": None, "algorithmic_bytes_per_step": algo_bytes,
+                     "peak_source": src, "traffic": recorded_traffic(name),
+                     "algorithmic_bytes_per_step": algo_bytes,
                      "kernel": f"splitkv_partial_kernel<{d},paged> + splitkv_merge_kernel<{d}>"},
         "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
     }), flush=True)

@@ -174,6 +174,7 @@ def config_inputs(name: str, compiled: bool = True):
 # Decode-shaped workloads for the split-KV path: Nq queries (the newest
 # positions) against Nk cached keys; K and V far larger than the 129 MB L2.
 DECODE_CONFIGS = {
+    "dec0": dict(B=4, H=32, Nq=1, Nk=16384, d=128, causal=False, seed=10),  # 1 GB: profiling size
     "dec1": dict(B=8, H=32, Nq=1, Nk=32768, d=128, causal=False, seed=5),
     "dec2": dict(B=1, H=32, Nq=4, Nk=131072, d=128, causal=True, seed=6),
     "dec3": dict(B=16, H=16, Nq=8, Nk=8192, d=64, causal=True, seed=7),

@@ -15,9 +15,11 @@
 //               producer/consumer tokens of the Triton warp-specialisation
 //               notes: acquire -> expect bytes -> TMA copy; consumer waits
 //               -> uses -> releases).
-//   warp 1      MMA issuer (one thread): S_j(s) = Q_s K_j^T with
-//               tcgen05.mma into TMEM, then O(s) += P_j(s) V_j with P read
-//               straight from TMEM.  Also allocates / frees TMEM.
+//   warp 1      MMA issuer: S_j(s) = Q_s K_j^T with tcgen05.mma into
+//               TMEM, then O(s) += P_j(s) V_j with P read straight from
+//               TMEM.  The whole warp runs the issue loop (so descriptors and
+//               loop state are warp-uniform) and one elected lane issues
+//               each batch of MMAs and commits.  Also allocates / frees TMEM.
 //   warps 4-7   softmax warpgroup for Q tile 0 (TMEM lanes 0-127, one query
 //   warps 8-11  row per thread), softmax warpgroup for Q tile 1.  Each reads
 //               its S row from TMEM, masks, updates m and l, writes P (bf16)
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    {
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, C::kBlockN, 0, 0);
       constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(128, D, 0, 1);
       const uint32_t tS0 = tmem + C::kColS0, tS1 = tmem + C::kColS1;
@@ -203,6 +205,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // carries out of it because every operand lies below 256 KiB.  The
       // single issuing thread is the tensor core's only feeder, so keeping
       // its per-MMA work to an add and the instruction itself matters.
+      // Every lane of the warp runs this loop with the same values; that
+      // keeps them warp-uniform, and an elected lane issues.
       // Q and K tiles: K-major, 128-byte swizzle, 8-row groups 1 KiB apart.
       const uint64_t dQ0 = ptx::desc_sw128(sQ(0), 16, 1024), dQ1 = ptx::desc_sw128(sQ(1), 16, 1024);
       const uint64_t dK0 = ptx::desc_sw128(sKV(0), 16, 1024);
@@ -217,26 +221,36 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const uint64_t dk = dK0 + slot_off(kslot);
         const uint64_t dq = s ? dQ1 : dQ0;
         const uint32_t ts = s ? tS1 : tS0;
+        if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t koff =
-              static_cast<uint64_t>(((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4);
-          ptx::mma_ss(ts, dq + koff, dk + koff, kIdescS, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t koff =
+                static_cast<uint64_t>(((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4);
+            ptx::mma_ss(ts, dq + koff, dk + koff, kIdescS, kk > 0 ? 1u : 0u);
+          }
         }
+        __syncwarp();
       };
       // O(s) += P(s) V over 128 keys in steps of 16; P read from TMEM
       auto issue_pv = [&](int s, int vslot, bool first) {
         const uint64_t dv = dV0 + slot_off(vslot);
         const uint32_t ts = s ? tS1 : tS0;
         const uint32_t to = s ? tO1 : tO0;
+        if (ptx::elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < C::kBlockN / 16; ++kk)
-          ptx::mma_ts(to, ts + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4), kIdescO,
-                      (!first || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < C::kBlockN / 16; ++kk)
+            ptx::mma_ts(to, ts + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                        kIdescO, (!first || kk > 0) ? 1u : 0u);
+        }
+        __syncwarp();
+      };
+      auto commit = [&](uint32_t b) {
+        if (ptx::elect_one()) ptx::mma_commit(b);
+        __syncwarp();
       };
       bool ok = true;
       for (int s = 0; s < 2 && ok; ++s)
-        if (n_s(s) > 0) ok = wait_one(q_full(s), 0, ctl, kSiteMmaQ);
+        if (n_s(s) > 0) ok = wait_warp(q_full(s), 0, ctl, kSiteMmaQ);
       int t = 0;
       int v_prev = 0;
       for (int j = 0; j < n_kv && ok; ++j) {
@@ -244,30 +258,30 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         ++t;
         const int v_slot = t % C::kStages, v_par = (t / C::kStages) & 1;
         ++t;
-        if (!wait_one(kv_full(k_slot), k_par, ctl, kSiteMmaKV)) {
+        if (!wait_warp(kv_full(k_slot), k_par, ctl, kSiteMmaKV)) {
           ok = false;
           break;
         }
         ptx::tc_fence_after();
         for (int s = 0; s < 2 && ok; ++s) {
           if (j >= 1 && j - 1 < n_s(s)) {
-            if (!wait_one(p_ready(s), (j - 1) & 1, ctl, kSiteMmaP)) {
+            if (!wait_warp(p_ready(s), (j - 1) & 1, ctl, kSiteMmaP)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
             issue_pv(s, v_prev, j - 1 == 0);
-            if (j - 1 == n_s(s) - 1) ptx::mma_commit(o_full(s));
+            if (j - 1 == n_s(s) - 1) commit(o_full(s));
           }
           if (j < n_s(s)) {
             issue_s(s, k_slot);
-            ptx::mma_commit(s_full(s));
+            commit(s_full(s));
           }
         }
         if (!ok) break;
-        ptx::mma_commit(kv_empty(k_slot));
-        if (j >= 1) ptx::mma_commit(kv_empty(v_prev));
-        if (!wait_one(kv_full(v_slot), v_par, ctl, kSiteMmaKV)) {
+        commit(kv_empty(k_slot));
+        if (j >= 1) commit(kv_empty(v_prev));
+        if (!wait_warp(kv_full(v_slot), v_par, ctl, kSiteMmaKV)) {
           ok = false;
           break;
         }
@@ -277,20 +291,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       if (ok) {
         for (int s = 0; s < 2 && ok; ++s) {
           if (n_kv - 1 < n_s(s)) {
-            if (!wait_one(p_ready(s), (n_kv - 1) & 1, ctl, kSiteMmaP)) {
+            if (!wait_warp(p_ready(s), (n_kv - 1) & 1, ctl, kSiteMmaP)) {
               ok = false;
               break;
             }
             ptx::tc_fence_after();
             issue_pv(s, v_prev, n_kv - 1 == 0);
-            ptx::mma_commit(o_full(s));
+            commit(o_full(s));
           }
         }
-        if (ok) ptx::mma_commit(kv_empty(v_prev));
+        if (ok) commit(kv_empty(v_prev));
       }
-      // every MMA this thread issued completes before TMEM is released
-      ptx::mma_commit(drain_bar);
-      drain_wait(drain_bar, 0, ctl);
+      // every MMA this warp issued completes before TMEM is released
+      commit(drain_bar);
+      if (lane == 0) drain_wait(drain_bar, 0, ctl);
     }
     __syncwarp();
   } else if (warp >= 4) {

@@ -56,6 +56,9 @@ __device__ __forceinline__ bool wait_one(uint32_t bar, uint32_t parity, const Wa
 // on to execute .sync.aligned tcgen05 instructions together).
 __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const WaitCtl& c,
                                           unsigned site) {
+  // the clock is read only once the first probe has failed: on the fast
+  // path (barrier already complete) it would be most of the cost
+  if (__all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
   const long long t0 = clock64();
   while (true) {
     const uint32_t ok = ptx::mbar_try_wait(bar, parity);

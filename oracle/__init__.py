@@ -1,4 +1,5 @@
-"""TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle for attention forward.
+"""TEST INFRASTRUCTURE ONLY: the fp64 CPU oracle for attention forward
+(and its gradients).
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The library's product path never
@@ -55,6 +56,9 @@ def _load():
         lib.oracle_attention_kv.argtypes = [p, p, p, i64, i64, i64, ctypes.c_float, ctypes.c_int,
                                             p, p, ctypes.c_int]
         lib.oracle_attention_kv.restype = ctypes.c_int
+        lib.oracle_attention_bwd.argtypes = [p, p, p, p, i64, i64, i64, ctypes.c_float, ctypes.c_int,
+                                             p, p, p, ctypes.c_int]
+        lib.oracle_attention_bwd.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -154,3 +158,21 @@ def attention_kv(q, k, v, scale: float, causal: bool, nthreads: int = 0):
         o[b, h] = ob
         lse[b, h] = lb
     return o, lse
+
+
+def attention_bwd(q, k, v, dout, scale: float, causal: bool, nthreads: int = 0):
+    """dQ, dK, dV [B,H,N,d] float64: the gradients of sum(dout * O) for the
+    attention output O of ``attention_fwd`` (same scale and mask)."""
+    q, k, v, dout = _bits(q), _bits(k), _bits(v), _bits(dout)
+    if not (q.shape == k.shape == v.shape == dout.shape) or q.ndim != 4:
+        raise ValueError("q, k, v, dout must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    dq = np.zeros((B, H, N, d), dtype=np.float64)
+    dk = np.zeros_like(dq)
+    dv = np.zeros_like(dq)
+    rc = _load().oracle_attention_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), B * H, N, d,
+                                      ctypes.c_float(scale), int(bool(causal)),
+                                      _ptr(dq), _ptr(dk), _ptr(dv), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_attention_bwd failed")
+    return dq, dk, dv

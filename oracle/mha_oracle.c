@@ -1,5 +1,6 @@
 /* TEST INFRASTRUCTURE ONLY.  A plain, slow fp64 CPU oracle for the
- * multi-head attention forward pass.  Only the tests, the smoke check and
+ * multi-head attention forward pass (and, at the end of the file, its
+ * gradients).  Only the tests, the smoke check and
  * the CPU-baseline leg of the benchmark load this file; the library's
  * product path never does, and the two share no code.
  *
@@ -106,13 +107,15 @@ int oracle_attention_rows(const uint16_t *q_bh, const uint16_t *k_bh, const uint
         if (!s) {
 #pragma omp atomic write
             bad = 1;
-        } else {
+        }
+        /* every thread reaches the work-sharing loop (a thread without its
+         * buffer takes no rows; the call then fails as a whole) */
 #pragma omp for schedule(dynamic, 4)
-            for (int64_t r = 0; r < nrows; ++r)
+        for (int64_t r = 0; r < nrows; ++r)
+            if (s)
                 attention_row(q_bh, k_bh, v_bh, N, d, (double)scale, causal, rows[r], s,
                               o_out + r * d, lse_out + r, NULL);
-            free(s);
-        }
+        free(s);
     }
     return bad ? -1 : 0;
 }
@@ -179,17 +182,114 @@ int oracle_attention_kv(const uint16_t *q_bh, const uint16_t *k_bh, const uint16
         if (!s) {
 #pragma omp atomic write
             bad = 1;
-        } else {
-#pragma omp for schedule(dynamic, 1)
-            for (int64_t i = 0; i < Nq; ++i) {
-                int64_t nk = causal ? Nk - Nq + i + 1 : Nk;
-                if (nk < 0) nk = 0;
-                if (nk > Nk) nk = Nk;
-                attention_row_keys(q_bh + i * d, k_bh, v_bh, Nk, d, (double)scale, nk, s,
-                                   o_out + i * d, lse_out + i, NULL);
-            }
-            free(s);
         }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < Nq; ++i) {
+            if (!s) continue;
+            int64_t nk = causal ? Nk - Nq + i + 1 : Nk;
+            if (nk < 0) nk = 0;
+            if (nk > Nk) nk = Nk;
+            attention_row_keys(q_bh + i * d, k_bh, v_bh, Nk, d, (double)scale, nk, s,
+                               o_out + i * d, lse_out + i, NULL);
+        }
+        free(s);
     }
     return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------ backward
+ * Gradients of the loss L = sum_{i,c} dO_ic * O_ic with respect to q, k and
+ * v, where O is the attention output defined above (same scale, same key
+ * sets).  The pages give no attention backward; this is the derivative of
+ * the forward definition written out (chain rule through the softmax):
+ *
+ *   P_ij  = softmax_j(s_i)          s_ij = scale <q_i, k_j>,  j in J_i
+ *   D_i   = sum_c dO_ic O_ic
+ *   dP_ij = sum_c dO_ic v_jc
+ *   dS_ij = P_ij (dP_ij - D_i)      (softmax Jacobian applied to dP_i)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dQ_i  = scale sum_j dS_ij k_j
+ *   dK_j  = scale sum_i dS_ij q_i
+ *
+ * All in fp64 from the exact bf16 inputs; O and P are recomputed exactly
+ * here (not taken from any kernel).  Query rows are split among threads;
+ * each thread accumulates its own dK / dV and the partials are summed.
+ * q, k, v, dout: [N, d] bf16 bits of one head; dq, dk, dv: [N, d] doubles. */
+static int attention_bwd_head(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                              const uint16_t *dout, int64_t N, int64_t d, double scale,
+                              int causal, double *dq, double *dk, double *dv, int nthreads) {
+    for (int64_t x = 0; x < N * d; ++x) dq[x] = dk[x] = dv[x] = 0.0;
+    if (N == 0) return 0;
+    int bad = 0;
+#pragma omp parallel num_threads(nthreads)
+    {
+        double *s = (double *)malloc(sizeof(double) * (size_t)N);
+        double *p = (double *)malloc(sizeof(double) * (size_t)N);
+        double *o = (double *)malloc(sizeof(double) * (size_t)d);
+        double *dk_t = (double *)calloc((size_t)(N * d), sizeof(double));
+        double *dv_t = (double *)calloc((size_t)(N * d), sizeof(double));
+        const int mine = s && p && o && dk_t && dv_t;
+        if (!mine) {
+#pragma omp atomic write
+            bad = 1;
+        }
+        /* every thread reaches the work-sharing loop; one without buffers
+         * takes no rows (the call then fails as a whole) */
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t i = 0; i < N; ++i) {
+            if (!mine) continue;
+            const uint16_t *q_row = q + i * d;
+            const uint16_t *do_row = dout + i * d;
+            double lse;
+            int64_t nk = causal ? i + 1 : N;
+            attention_row_keys(q_row, k, v, N, d, scale, nk, s, o, &lse, p);
+            double D = 0.0;
+            for (int64_t c = 0; c < d; ++c) D += bf16_to_f64(do_row[c]) * o[c];
+            for (int64_t j = 0; j < nk; ++j) {
+                double dp = 0.0;
+                for (int64_t c = 0; c < d; ++c)
+                    dp += bf16_to_f64(do_row[c]) * bf16_to_f64(v[j * d + c]);
+                const double ds = p[j] * (dp - D);
+                for (int64_t c = 0; c < d; ++c) {
+                    dq[i * d + c] += scale * ds * bf16_to_f64(k[j * d + c]);
+                    dk_t[j * d + c] += scale * ds * bf16_to_f64(q_row[c]);
+                    dv_t[j * d + c] += p[j] * bf16_to_f64(do_row[c]);
+                }
+            }
+        }
+        if (mine) {
+#pragma omp critical
+            {
+                for (int64_t x = 0; x < N * d; ++x) {
+                    dk[x] += dk_t[x];
+                    dv[x] += dv_t[x];
+                }
+            }
+        }
+        free(s);
+        free(p);
+        free(o);
+        free(dk_t);
+        free(dv_t);
+    }
+    return bad ? -1 : 0;
+}
+
+/* Every head: q, k, v, dout [BH, N, d]; dq, dk, dv [BH, N, d] doubles. */
+int oracle_attention_bwd(const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                         const uint16_t *dout, int64_t BH, int64_t N, int64_t d, float scale,
+                         int causal, double *dq, double *dk, double *dv, int nthreads) {
+    if (BH < 0 || N < 0 || d <= 0) return -1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#else
+    nthreads = 1;
+#endif
+    for (int64_t bh = 0; bh < BH; ++bh) {
+        const int64_t off = bh * N * d;
+        if (attention_bwd_head(q + off, k + off, v + off, dout + off, N, d, (double)scale, causal,
+                               dq + off, dk + off, dv + off, nthreads) != 0)
+            return -1;
+    }
+    return 0;
 }

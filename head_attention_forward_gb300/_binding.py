@@ -57,6 +57,11 @@ def lib() -> ctypes.CDLL:
         L.mha_fwd_paged.restype = i
         L.mha_fwd_kv_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, f, i, i, vp]
         L.mha_fwd_kv_noalloc.restype = i
+        L.mha_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, f, i, vp,
+                              ctypes.c_size_t, vp]
+        L.mha_bwd.restype = i
+        L.mha_bwd_workspace_size.argtypes = [i, i, i, i]
+        L.mha_bwd_workspace_size.restype = ctypes.c_size_t
         _lib = L
     return _lib
 
@@ -178,3 +183,30 @@ def mha_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B: int, H:
                              _stream(stream))
     if rc != MHA_OK:
         raise MhaError(rc, "mha_fwd_paged")
+
+
+def mha_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(lib().mha_bwd_workspace_size(int(B), int(H), int(N), int(d)))
+
+
+def mha_bwd(q, k, v, o, lse, dout, dq, dk, dv, B: int, H: int, N: int, d: int, scale: float,
+            causal: bool, workspace, workspace_bytes: int, stream=None) -> None:
+    """C ``mha_bwd``: tensors (or raw device addresses) in, status checked."""
+    rc = lib().mha_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk),
+                       _ptr(dv), int(B), int(H), int(N), int(d), ctypes.c_float(scale),
+                       int(bool(causal)), _ptr(workspace), int(workspace_bytes), _stream(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_bwd")
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, stream=None):
+    """Allocate dQ, dK, dV and the workspace with torch and run ``mha_bwd``."""
+    import torch
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = float(torch.tensor(d, dtype=torch.float32).rsqrt())
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = mha_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    mha_bwd(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, stream)
+    return dq, dk, dv

@@ -8,7 +8,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 SOURCES = [os.path.join(CSRC, "mha_fwd.cu"), os.path.join(CSRC, "mha_splitkv.cu"),
-           os.path.join(CSRC, "mha_noalloc.cu")]
+           os.path.join(CSRC, "mha_noalloc.cu"), os.path.join(CSRC, "mha_bwd.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
 HEADERS.append(os.path.join(ROOT, "include", "mha_fwd.h"))
 LIB = os.path.join(PKG, "_build", "libmha_fwd.so")

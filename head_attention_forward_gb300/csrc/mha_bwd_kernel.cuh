@@ -1,0 +1,419 @@
+// mha_bwd_kernel.cuh - attention backward for sm_103a (GB300).
+//
+// What it computes: the gradients of L = sum(dO * O) with respect to Q, K and
+// V for the forward pass of mha_fwd_kernel.cuh (same scale, same square
+// top-left causal mask).  The pages give no attention backward; this is the
+// derivative of the forward definition (chain rule through the row softmax),
+// organised the FlashAttention-2 way: P is recomputed from the saved
+// log-sum-exp instead of being stored.  Per head, with P_ij =
+// exp(scale q_i.k_j - LSE_i) on the visible keys:
+//
+//   D_i   = sum_c dO_ic O_ic                       (bwd_rowdot_kernel)
+//   dV_j  = sum_i P_ij dO_i                        (bwd_dkdv_kernel)
+//   dS_ij = P_ij (dO_i.v_j - D_i)
+//   dK_j  = scale sum_i dS_ij q_i                  (bwd_dkdv_kernel)
+//   dQ_i  = scale sum_j dS_ij k_j                  (bwd_dq_kernel)
+//
+// dK/dV and dQ are computed by two kernels that each recompute the scores
+// they need (S^T and dP^T per key tile in one, S and dP per query tile in
+// the other), so no partial sum ever goes through global atomics.
+//
+// Both kernels share the forward kernel's shape: warp 0 feeds tiles with TMA
+// through mbarrier-guarded shared-memory slots, warp 1 allocates TMEM and
+// runs the tcgen05.mma issue loop (whole warp, one elected lane issues),
+// warps 4-7 own one TMEM lane (one row of the tile) per thread and do the
+// elementwise work; warps 2-3 only keep warps 4-7 on TMEM lane quarters.
+// P (or dS) is written back to TMEM as bf16 over the scores it came from and
+// is the A operand of the next MMA straight from TMEM.
+//
+// Every mbarrier wait is bounded (see mha_wait.cuh); a wait that runs out
+// records a status bit, raises the CTA's abort flag, and the CTA drains its
+// own copies and MMAs before freeing TMEM.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "mha_wait.cuh"
+#include "sm103_ptx.cuh"
+
+namespace mha {
+
+struct BwdParams {
+  const float* lse;        // [BH, N] natural log, from the forward pass
+  const float* dsum;       // [BH, N] D_i (workspace, written by bwd_rowdot_kernel)
+  __nv_bfloat16* dq;       // [BH, N, D]
+  __nv_bfloat16* dk;       // [BH, N, D]
+  __nv_bfloat16* dv;       // [BH, N, D]
+  unsigned* status;        // device status word
+  long long wait_limit;    // SM cycles per wait
+  int N;
+  int n_tiles;             // ceil(N / 128)
+  float scale;             // score multiplier
+  float scale_log2;        // scale * log2(e)
+};
+
+template <int D>
+struct BwdCfg {
+  static_assert(D == 64 || D == 128, "head dimension");
+  static constexpr int kBlock = 128;             // rows per tile (queries or keys)
+  static constexpr int kHalves = D / 64;         // 128-byte swizzle atoms across d
+  static constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 bytes
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kRing = (D == 128) ? 2 : 3;  // slots of two tiles each
+  // fixed pair (K,V for dK/dV; Q,dO for dQ), then the ring of pairs
+  static constexpr int kOffFixed = 0;
+  static constexpr int kOffRing = 2 * kTileBytes;
+  static constexpr int kOffRowBuf = kOffRing + kRing * 2 * kTileBytes;  // float2 [4 warps][128]
+  static constexpr int kOffBar = kOffRowBuf + 4 * 128 * 8;
+  // barriers: fixed_full ring_full[R] ring_empty[R] s_full p_ready acc_full drain
+  static constexpr int kBarFixed = 0, kBarRingFull = 1, kBarRingEmpty = 1 + kRing;
+  static constexpr int kBarSFull = 1 + 2 * kRing, kBarPReady = kBarSFull + 1;
+  static constexpr int kBarAcc = kBarPReady + 1, kBarDrain = kBarAcc + 1;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+  static constexpr int kOffAbort = kOffTmemSlot + 4;
+  static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+  static_assert(kOffBar % 8 == 0 && kOffRing % 1024 == 0, "mbarrier / swizzle-atom alignment");
+  static constexpr int kThreads = 256;
+  static constexpr uint32_t kTmemCols = 512;
+  // scores [0,128), second product [128,256), accumulators from 256
+  static constexpr uint32_t kColS = 0, kColP2 = 128, kColAcc = 256;
+};
+
+// D_i = sum_c dO_ic O_ic in fp32: one warp per row, rows [BH * N).
+template <int D>
+__global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
+                                                         const __nv_bfloat16* __restrict__ dout,
+                                                         float* __restrict__ dsum,
+                                                         long long rows) {
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  constexpr int kPer = D / 32;  // elements per lane: 2 or 4
+  const __nv_bfloat16* a = o + row * D + lane * kPer;
+  const __nv_bfloat16* b = dout + row * D + lane * kPer;
+  float acc = 0.f;
+  if constexpr (kPer == 4) {
+    const uint2 ua = *reinterpret_cast<const uint2*>(a);
+    const uint2 ub = *reinterpret_cast<const uint2*>(b);
+    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ua.x));
+    const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ua.y));
+    const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ub.x));
+    const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ub.y));
+    acc = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
+  } else {
+    const uint32_t ua = *reinterpret_cast<const uint32_t*>(a);
+    const uint32_t ub = *reinterpret_cast<const uint32_t*>(b);
+    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ua));
+    const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ub));
+    acc = a0.x * b0.x + a0.y * b0.y;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) dsum[row] = acc;
+}
+
+// Shared skeleton of the two tile kernels.  DKDV = true: one CTA per
+// (batch*head, 128-key tile); the fixed pair is (K, V) and the ring carries
+// (Q_i, dO_i) for every query tile that sees these keys.  DKDV = false: one
+// CTA per (batch*head, 128-query tile); the fixed pair is (Q, dO) and the
+// ring carries (K_j, V_j).
+template <int D, bool CAUSAL, bool DKDV>
+__global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
+    bwd_tile_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                    const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = ptx::smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = ptx::smem_u32(smem);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int N = p.N;
+  // this CTA's own tile (keys for dK/dV, queries for dQ), heaviest first
+  // under the causal mask
+  const int tile = (CAUSAL && !DKDV) ? (p.n_tiles - 1 - static_cast<int>(blockIdx.y))
+                                     : static_cast<int>(blockIdx.y);
+  const int r0 = tile * C::kBlock;
+  // the other side's tiles this CTA walks: [t_begin, t_end)
+  const int t_begin = (CAUSAL && DKDV) ? tile : 0;
+  const int t_end = (CAUSAL && !DKDV) ? tile + 1 : p.n_tiles;
+  const int n_steps = t_end - t_begin;
+
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
+  const uint32_t fixed_full = bar(C::kBarFixed);
+  auto ring_full = [&](int i) { return bar(C::kBarRingFull + i); };
+  auto ring_empty = [&](int i) { return bar(C::kBarRingEmpty + i); };
+  const uint32_t s_full = bar(C::kBarSFull);
+  const uint32_t p_ready = bar(C::kBarPReady);
+  const uint32_t acc_full = bar(C::kBarAcc);
+  const uint32_t drain_bar = bar(C::kBarDrain);
+  // fixed pair: [0] K or Q, [1] V or dO; ring slot i: [0] Q or K, [1] dO or V
+  auto sFixed = [&](int w) -> uint32_t { return sbase + C::kOffFixed + w * C::kTileBytes; };
+  auto sRing = [&](int i, int w) -> uint32_t {
+    return sbase + C::kOffRing + (2 * i + w) * C::kTileBytes;
+  };
+
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
+  const WaitCtl ctl{abort_flag, p.status, p.wait_limit};
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(fixed_full, 1);
+    for (int i = 0; i < C::kRing; ++i) {
+      ptx::mbar_init(ring_full(i), 1);
+      ptx::mbar_init(ring_empty(i), 1);
+    }
+    ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(p_ready, 4);  // one elected arrive per elementwise warp
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tensormap(&tmQ);
+    ptx::prefetch_tensormap(&tmK);
+    ptx::prefetch_tensormap(&tmV);
+    ptx::prefetch_tensormap(&tmDO);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const CUtensorMap* fixed0 = DKDV ? &tmK : &tmQ;
+  const CUtensorMap* fixed1 = DKDV ? &tmV : &tmDO;
+  const CUtensorMap* ring0 = DKDV ? &tmQ : &tmK;
+  const CUtensorMap* ring1 = DKDV ? &tmDO : &tmV;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_steps > 0) {
+      ptx::mbar_arrive_expect_tx(fixed_full, 2 * C::kTileBytes);
+      for (int h = 0; h < C::kHalves; ++h) {
+        ptx::tma_load_3d(sFixed(0) + h * C::kHalfBytes, fixed0, fixed_full, h * 64, r0, bh);
+        ptx::tma_load_3d(sFixed(1) + h * C::kHalfBytes, fixed1, fixed_full, h * 64, r0, bh);
+      }
+      int t = 0;
+      bool ok = true;
+      for (; t < n_steps; ++t) {
+        const int slot = t % C::kRing;
+        const int use = t / C::kRing;
+        if (use > 0 && !wait_one(ring_empty(slot), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
+          ok = false;
+          break;
+        }
+        const int y = (t_begin + t) * C::kBlock;
+        ptx::mbar_arrive_expect_tx(ring_full(slot), 2 * C::kTileBytes);
+        for (int h = 0; h < C::kHalves; ++h) {
+          ptx::tma_load_3d(sRing(slot, 0) + h * C::kHalfBytes, ring0, ring_full(slot), h * 64, y, bh);
+          ptx::tma_load_3d(sRing(slot, 1) + h * C::kHalfBytes, ring1, ring_full(slot), h * 64, y, bh);
+        }
+      }
+      if (!ok) {
+        // let the copies already issued land before the CTA goes away
+        drain_wait(fixed_full, 0, ctl);
+        for (int u = max(0, t - C::kRing); u < t; ++u)
+          drain_wait(ring_full(u % C::kRing), (u / C::kRing) & 1, ctl);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------- MMA issuer
+    // Every lane runs the loop with the same values; an elected lane issues.
+    constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t kIdescAcc = ptx::idesc_bf16_f32(128, D, 0, 1);
+    const uint32_t tS = tmem + C::kColS, tP2 = tmem + C::kColP2;
+    const uint32_t tAcc0 = tmem + C::kColAcc, tAcc1 = tmem + C::kColAcc + D;
+    // K-major views (rows x d, 128-byte swizzle, 8-row groups 1 KiB apart)
+    // and MN-major views (d contiguous, d-halves 16 KiB apart) of a tile
+    auto kmaj = [](uint32_t a) { return ptx::desc_sw128(a, 16, 1024); };
+    auto mnmaj = [](uint32_t a) { return ptx::desc_sw128(a, C::kHalfBytes, 1024); };
+    // dst[128 x 128] = a_tile . b_tile^T over d
+    auto issue_scores = [&](uint32_t dst, uint32_t a_tile, uint32_t b_tile) {
+      const uint64_t da = kmaj(a_tile), db = kmaj(b_tile);
+      if (ptx::elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t koff =
+              static_cast<uint64_t>(((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4);
+          ptx::mma_ss(dst, da + koff, db + koff, kIdescS, kk > 0 ? 1u : 0u);
+        }
+      }
+      __syncwarp();
+    };
+    // acc[128 x D] (+)= A . b_tile, A (128 x 128, bf16) read from TMEM at a_cols
+    auto issue_acc = [&](uint32_t acc, uint32_t a_cols, uint32_t b_tile, bool first) {
+      const uint64_t db = mnmaj(b_tile);
+      if (ptx::elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < C::kBlock / 16; ++kk)
+          ptx::mma_ts(acc, a_cols + kk * 8, db + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                      kIdescAcc, (!first || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+    };
+    auto commit = [&](uint32_t b) {
+      if (ptx::elect_one()) ptx::mma_commit(b);
+      __syncwarp();
+    };
+    bool ok = n_steps > 0 && wait_warp(fixed_full, 0, ctl, kSiteMmaQ);
+    for (int t = 0; t < n_steps && ok; ++t) {
+      const int slot = t % C::kRing;
+      if (!(ok = wait_warp(ring_full(slot), (t / C::kRing) & 1, ctl, kSiteMmaKV))) break;
+      ptx::tc_fence_after();
+      if constexpr (DKDV) {
+        issue_scores(tS, sFixed(0), sRing(slot, 0));   // S^T  = K  Q_i^T
+        issue_scores(tP2, sFixed(1), sRing(slot, 1));  // dP^T = V  dO_i^T
+      } else {
+        issue_scores(tS, sFixed(0), sRing(slot, 0));   // S  = Q  K_j^T
+        issue_scores(tP2, sFixed(1), sRing(slot, 1));  // dP = dO V_j^T
+      }
+      commit(s_full);
+      if (!(ok = wait_warp(p_ready, t & 1, ctl, kSiteMmaP))) break;
+      ptx::tc_fence_after();
+      if constexpr (DKDV) {
+        issue_acc(tAcc0, tS, sRing(slot, 1), t == 0);   // dV += P^T  dO_i
+        issue_acc(tAcc1, tP2, sRing(slot, 0), t == 0);  // dK += dS^T Q_i
+      } else {
+        issue_acc(tAcc0, tS, sRing(slot, 0), t == 0);   // dQ += dS K_j
+      }
+      commit(ring_empty(slot));
+    }
+    if (ok) commit(acc_full);
+    // every MMA this warp issued completes before TMEM is released
+    commit(drain_bar);
+    if (lane == 0) drain_wait(drain_bar, 0, ctl);
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ elementwise rows
+    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = wq * 32 + lane;
+    const int my = r0 + row;  // this thread's key (dK/dV) or query (dQ)
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::kColS, tP2 = tmem + lane_off + C::kColP2;
+    const float sl2 = p.scale_log2;
+    constexpr float kLog2e = 1.4426950408889634f;
+    const size_t base = static_cast<size_t>(bh) * N;
+    // per-warp copy of the current query tile's (LSE * log2 e, D) (dK/dV)
+    float2* rowbuf = reinterpret_cast<float2*>(smem + C::kOffRowBuf) + (warp - 4) * 128;
+    // this row's own (LSE * log2 e, D) (dQ); rows past N see no key
+    float my_lse2 = INFINITY, my_d = 0.f;
+    if (!DKDV && my < N) {
+      my_lse2 = p.lse[base + my] * kLog2e;
+      my_d = p.dsum[base + my];
+    }
+    bool ok = true;
+    for (int t = 0; t < n_steps && ok; ++t) {
+      const int y0 = (t_begin + t) * C::kBlock;  // first column's query (dK/dV) or key (dQ)
+      if constexpr (DKDV) {
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int c = lane + 32 * m;
+          const int qi = y0 + c;
+          // a query past N has LSE = +inf here, so its P and dS are 0
+          rowbuf[c] = qi < N ? make_float2(p.lse[base + qi] * kLog2e, p.dsum[base + qi])
+                             : make_float2(INFINITY, 0.f);
+        }
+        __syncwarp();
+      }
+      if (!wait_warp(s_full, t & 1, ctl, kSiteSoftmaxS)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+      // four 32-column chunks; chunk k's bf16 results go to columns
+      // [16k, 16k + 16), all of which earlier loads have already read
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
+        uint32_t sr[32], dr[32];
+        ptx::tmem_ld_x32(tS + 32 * k, sr);
+        ptx::tmem_ld_x32(tP2 + 32 * k, dr);
+        uint32_t pk_p[16], pk_ds[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float pp[2], dd[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int c = 32 * k + 2 * i + e;
+            float lse2, dsum;
+            bool vis;
+            if constexpr (DKDV) {
+              const float2 ld = rowbuf[c];
+              lse2 = ld.x;
+              dsum = ld.y;
+              vis = !CAUSAL || my <= y0 + c;  // key my, query y0 + c
+            } else {
+              lse2 = my_lse2;
+              dsum = my_d;
+              const int key = y0 + c;
+              vis = key < N && (!CAUSAL || key <= my);
+            }
+            const float pe = vis ? ptx::ex2(__uint_as_float(sr[2 * i + e]) * sl2 - lse2) : 0.f;
+            pp[e] = pe;
+            dd[e] = pe * (__uint_as_float(dr[2 * i + e]) - dsum);
+          }
+          pk_p[i] = ptx::pack_bf16x2(pp[0], pp[1]);
+          pk_ds[i] = ptx::pack_bf16x2(dd[0], dd[1]);
+        }
+        if constexpr (DKDV) {
+          ptx::tmem_st_x16(tS + 16 * k, pk_p);    // P^T  over S^T
+          ptx::tmem_st_x16(tP2 + 16 * k, pk_ds);  // dS^T over dP^T
+        } else {
+          ptx::tmem_st_x16(tS + 16 * k, pk_ds);   // dS over S
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(p_ready);
+    }
+    if (ok && n_steps > 0 && wait_warp(acc_full, 0, ctl, kSiteSoftmaxO)) {
+      ptx::tc_fence_after();
+      const bool valid = my < N;
+      // epilogue: accumulators -> bf16 rows (dK and dQ carry the scale)
+#pragma unroll 1
+      for (int which = 0; which < (DKDV ? 2 : 1); ++which) {
+        __nv_bfloat16* out = DKDV ? (which == 0 ? p.dv : p.dk) : p.dq;
+        const float mul = (DKDV && which == 0) ? 1.f : p.scale;
+        const uint32_t tacc = tmem + lane_off + C::kColAcc + which * D;
+        __nv_bfloat16* orow = out + (base + (valid ? my : 0)) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t av[32];
+          ptx::tmem_ld_x32(tacc + c * 32, av);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = ptx::pack_bf16x2(__uint_as_float(av[2 * i]) * mul,
+                                     __uint_as_float(av[2 * i + 1]) * mul);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace mha

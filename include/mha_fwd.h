@@ -165,6 +165,44 @@ int mha_fwd_kv_noalloc(const void *q, const void *k, const void *v, void *o, flo
                        int B, int H, int Nq, int Nk, int d, float scale, int causal,
                        int num_splits, void *stream);
 
+/*
+ * mha_bwd - gradients of the attention forward pass (mha_fwd) with respect
+ * to q, k and v, for a loss whose gradient with respect to O is dout.
+ *
+ * The pages describe the forward pass only; these are the derivatives of
+ * its definition (chain rule through the row softmax), in the
+ * FlashAttention-2 arrangement that recomputes P from the saved LSE.  For
+ * each batch b, head h, with P_ij = exp(scale <q_i, k_j> - LSE_i) on the key
+ * set J_i of mha_fwd (and 0 elsewhere):
+ *
+ *     D_i   = sum_c dout_ic O_ic
+ *     dS_ij = P_ij (<dout_i, v_j> - D_i)
+ *     dq_i  = scale sum_j dS_ij k_j
+ *     dk_j  = scale sum_i dS_ij q_i
+ *     dv_j  = sum_i P_ij dout_i
+ *
+ *   q, k, v    : bf16 [B, H, N, d], device, the forward inputs.
+ *   o, lse     : the forward outputs of mha_fwd for these inputs (bf16
+ *                [B, H, N, d] and fp32 [B, H, N]); they are used as given.
+ *   dout       : bf16 [B, H, N, d], device, gradient of the loss w.r.t. O.
+ *   dq, dk, dv : bf16 [B, H, N, d], device, written.
+ *   d, scale, causal : as passed to mha_fwd.
+ *   workspace, workspace_bytes : device scratch owned by the caller, at
+ *                least mha_bwd_workspace_size(B, H, N, d) bytes (fp32 D_i
+ *                per row); contents need no initialisation.
+ *   stream     : cudaStream_t; three kernels are queued on it.
+ *
+ * Every pointer must be non-NULL and 16-byte aligned; the three outputs and
+ * the workspace must not overlap each other or any input.  B*H*N == 0 is a
+ * no-op.  Errors as for mha_fwd.
+ */
+int mha_bwd(const void *q, const void *k, const void *v, const void *o, const float *lse,
+            const void *dout, void *dq, void *dk, void *dv, int B, int H, int N, int d,
+            float scale, int causal, void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes mha_bwd needs (0 for invalid arguments).  No CUDA call. */
+size_t mha_bwd_workspace_size(int B, int H, int N, int d);
+
 /* A short, static, human-readable description of a status code. */
 const char *mha_strerror(int status);
 

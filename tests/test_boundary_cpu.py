@@ -147,3 +147,37 @@ def test_paged_argument_checks(L):
     assert call(d=80) == mha.MHA_ERR_UNSUPPORTED_DIM
     assert call(wsb=8) == mha.MHA_ERR_INVALID_ARG
     assert call(Nq=0) == mha.MHA_OK
+
+
+def test_bwd_workspace_size_is_pure():
+    import head_attention_forward_gb300 as mha
+    assert mha.mha_bwd_workspace_size(2, 3, 100, 128) == (2 * 3 * 100 * 4 + 15) // 16 * 16
+    assert mha.mha_bwd_workspace_size(1, 1, 7, 64) == 32
+    assert mha.mha_bwd_workspace_size(1, 1, 7, 96) == 0
+    assert mha.mha_bwd_workspace_size(-1, 1, 7, 64) == 0
+    assert mha.mha_bwd_workspace_size(0, 1, 7, 64) == 0
+
+
+def test_bwd_argument_checks(L):
+    import head_attention_forward_gb300 as mha
+    big = 1 << 40
+    a = dict(q=big, k=2 * big, v=3 * big, o=4 * big, lse=5 * big, do=6 * big, dq=7 * big,
+             dk=8 * big, dv=9 * big, B=1, H=2, N=100, d=64, scale=0.125, causal=1, ws=10 * big,
+             wsb=1 << 20)
+
+    def call(**kw):
+        x = dict(a, **kw)
+        return L.mha_bwd(x["q"], x["k"], x["v"], x["o"], x["lse"], x["do"], x["dq"], x["dk"],
+                         x["dv"], x["B"], x["H"], x["N"], x["d"], ctypes.c_float(x["scale"]),
+                         x["causal"], x["ws"], x["wsb"], None)
+    assert call(d=96) == mha.MHA_ERR_UNSUPPORTED_DIM
+    assert call(N=-1) == mha.MHA_ERR_INVALID_ARG
+    assert call(scale=0.0) == mha.MHA_ERR_INVALID_ARG
+    assert call(do=0) == mha.MHA_ERR_INVALID_ARG
+    assert call(ws=0) == mha.MHA_ERR_INVALID_ARG
+    assert call(dk=8 * big + 8) == mha.MHA_ERR_MISALIGNED
+    assert call(wsb=16) == mha.MHA_ERR_INVALID_ARG             # workspace too small
+    assert call(dq=big) == mha.MHA_ERR_INVALID_ARG             # dq over q
+    assert call(dv=7 * big) == mha.MHA_ERR_INVALID_ARG         # dv over dq
+    assert call(ws=9 * big) == mha.MHA_ERR_INVALID_ARG         # workspace over dv
+    assert call(N=0) == mha.MHA_OK and call(B=0) == mha.MHA_OK

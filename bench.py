@@ -394,6 +394,85 @@ def run_paged(args, name):
     }), flush=True)
     return 0
 
+BWD_METRIC = ("attention bwd TFLOP/s (counted 10*B*H*N^2*d, halved when causal) and % of GB300 "
+              "bf16 tensor peak, per (B,H,N,d,causal)")
+
+
+def run_backward(args, name):
+    """mha_bwd on a forward workload: O and LSE come from one mha_fwd call,
+    dO is a synthetic N(0,1) tensor; each step is one mha_bwd call (three
+    kernels).  Single GPU."""
+    import torch
+
+    import head_attention_forward_gb300 as mha
+    c = synth.CONFIGS[name]
+    B, H, N, d, causal = c["B"], c["H"], c["N"], c["d"], c["causal"]
+    torch.cuda.set_device(0)
+    mha.build()
+    mha.lib()
+    qb, kb, vb = synth.qkv(c["seed"], B, H, N, d, c["sigma_qk"], c["sigma_v"])
+    dob = synth.normal_bf16_c(c["seed"], 3, B * H * N * d).reshape(B, H, N, d)
+
+    def dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v, do = dev(qb), dev(kb), dev(vb), dev(dob)
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    stream = torch.cuda.current_stream()
+    sptr = int(stream.cuda_stream)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    mha.mha_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, sptr)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = mha.mha_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+
+    def step():
+        mha.mha_bwd(q, k, v, o, lse, do, dq, dk, dv, B, H, N, d, scale, causal, ws, ws_bytes, sptr)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    with ClockSampler(0) as clk:
+        torch.cuda.synchronize()
+        evs[0].record(stream)
+        for i in range(args.steps):
+            step()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+    rc, word = mha.mha_device_status(sptr)
+    if rc != mha.MHA_OK:
+        raise RuntimeError(f"device status {rc} ({word:#x})")
+    ms = evs[0].elapsed_time(evs[-1]) / args.steps
+    flops = 10.0 * B * H * N * N * d / (2 if causal else 1)
+    tf = flops / (ms * 1e-3) / 1e12
+    peak, peak_burst = 1703.5, 1891.4
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        with open(pk_path) as f:
+            pk = json.load(f)
+        peak = float(pk.get("bf16_tflops_sustained", peak))
+        peak_burst = float(pk.get("bf16_tflops", peak_burst))
+    print(json.dumps({
+        "metric": BWD_METRIC, "value": tf, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{name} backward: B={B},H={H},N={N},d={d},"
+                               f"{'causal' if causal else 'non-causal'}",
+                   "flops_per_step": flops,
+                   "l2": "inputs larger than L2" if 6 * B * H * N * d * 2 > 129e6 else
+                         "inputs smaller than L2 (not flushed)"},
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s",
+                     "frac": tf / peak, "peak_source": "measured (MEASURED_PEAKS.json: "
+                     "bf16_tflops_sustained; burst beside it)", "peak_burst": peak_burst,
+                     "frac_burst": tf / peak_burst, "traffic": None,
+                     "kernel": f"mha_bwd call: bwd_rowdot_kernel<{d}> + bwd_tile_kernel<{d}> x2 "
+                               "(counted FLOPs over the call's time)"},
+        "gpu_launches": 3 * args.steps, "clocks": clk.summary(),
+    }), flush=True)
+    return 0
+
 
 def main():
     ap = argparse.ArgumentParser()
@@ -406,8 +485,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--backward", action="store_true",
+                    help="time mha_bwd on the chosen forward workload instead of mha_fwd")
     args = ap.parse_args()
     name = args.config
+    if args.backward:
+        if name not in synth.CONFIGS:
+            ap.error("--backward takes one of the forward workloads")
+        return run_backward(args, name)
     if name in synth.DECODE_CONFIGS:
         return run_decode(args, name)
     if name in synth.PAGED_CONFIGS:

@@ -9,22 +9,23 @@
 // exp(scale q_i.k_j - LSE_i) on the visible keys:
 //
 //   D_i   = sum_c dO_ic O_ic                       (bwd_rowdot_kernel)
-//   dV_j  = sum_i P_ij dO_i                        (bwd_dkdv_kernel)
+//   dV_j  = sum_i P_ij dO_i                        (bwd_tile_kernel, DKDV)
 //   dS_ij = P_ij (dO_i.v_j - D_i)
-//   dK_j  = scale sum_i dS_ij q_i                  (bwd_dkdv_kernel)
-//   dQ_i  = scale sum_j dS_ij k_j                  (bwd_dq_kernel)
+//   dK_j  = scale sum_i dS_ij q_i                  (bwd_tile_kernel, DKDV)
+//   dQ_i  = scale sum_j dS_ij k_j                  (bwd_tile_kernel, !DKDV)
 //
-// dK/dV and dQ are computed by two kernels that each recompute the scores
-// they need (S^T and dP^T per key tile in one, S and dP per query tile in
-// the other), so no partial sum ever goes through global atomics.
+// dK/dV and dQ come from two instantiations of one tile kernel that each
+// recompute the scores they need (S^T and dP^T per key tile in one, S and dP
+// per query tile in the other), so no partial sum goes through global
+// atomics.
 //
 // Both kernels share the forward kernel's shape: warp 0 feeds tiles with TMA
 // through mbarrier-guarded shared-memory slots, warp 1 allocates TMEM and
 // runs the tcgen05.mma issue loop (whole warp, one elected lane issues),
 // warps 4-7 own one TMEM lane (one row of the tile) per thread and do the
 // elementwise work; warps 2-3 only keep warps 4-7 on TMEM lane quarters.
-// P (or dS) is written back to TMEM as bf16 over the scores it came from and
-// is the A operand of the next MMA straight from TMEM.
+// P^T is written back to TMEM as bf16 over S^T, and dS (dS^T) over dP
+// (dP^T); each is the A operand of a later MMA straight from TMEM.
 //
 // Every mbarrier wait is bounded (see mha_wait.cuh); a wait that runs out
 // records a status bit, raises the CTA's abort flag, and the CTA drains its
@@ -66,10 +67,13 @@ struct BwdCfg {
   static constexpr int kOffRing = 2 * kTileBytes;
   static constexpr int kOffRowBuf = kOffRing + kRing * 2 * kTileBytes;  // float2 [4 warps][128]
   static constexpr int kOffBar = kOffRowBuf + 4 * 128 * 8;
-  // barriers: fixed_full ring_full[R] ring_empty[R] s_full p_ready acc_full drain
+  // barriers: fixed_full ring_full[R] ring_empty[R] s_full dp_full p_ready
+  //           ds_ready acc_full drain
   static constexpr int kBarFixed = 0, kBarRingFull = 1, kBarRingEmpty = 1 + kRing;
-  static constexpr int kBarSFull = 1 + 2 * kRing, kBarPReady = kBarSFull + 1;
-  static constexpr int kBarAcc = kBarPReady + 1, kBarDrain = kBarAcc + 1;
+  static constexpr int kBarSFull = 1 + 2 * kRing, kBarDpFull = kBarSFull + 1;
+  // p_ready: P^T written back (dK/dV), or S read into registers (dQ)
+  static constexpr int kBarPReady = kBarDpFull + 1, kBarDsReady = kBarPReady + 1;
+  static constexpr int kBarAcc = kBarDsReady + 1, kBarDrain = kBarAcc + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -149,8 +153,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const uint32_t fixed_full = bar(C::kBarFixed);
   auto ring_full = [&](int i) { return bar(C::kBarRingFull + i); };
   auto ring_empty = [&](int i) { return bar(C::kBarRingEmpty + i); };
-  const uint32_t s_full = bar(C::kBarSFull);
+  const uint32_t s_full = bar(C::kBarSFull);    // scores in TMEM
+  const uint32_t dp_full = bar(C::kBarDpFull);  // dO.V products in TMEM
+  // dK/dV: P^T written back over S^T; dQ: S read into registers
   const uint32_t p_ready = bar(C::kBarPReady);
+  const uint32_t ds_ready = bar(C::kBarDsReady);  // dS (dS^T) written back over dP (dP^T)
   const uint32_t acc_full = bar(C::kBarAcc);
   const uint32_t drain_bar = bar(C::kBarDrain);
   // fixed pair: [0] K or Q, [1] V or dO; ring slot i: [0] Q or K, [1] dO or V
@@ -170,7 +177,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ptx::mbar_init(ring_empty(i), 1);
     }
     ptx::mbar_init(s_full, 1);
+    ptx::mbar_init(dp_full, 1);
     ptx::mbar_init(p_ready, 4);  // one elected arrive per elementwise warp
+    ptx::mbar_init(ds_ready, 4);
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -268,27 +277,49 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       __syncwarp();
     };
     bool ok = n_steps > 0 && wait_warp(fixed_full, 0, ctl, kSiteMmaQ);
+    // The scores of the next tile are computed while this tile's dS is being
+    // made, and the next dO.V product while its P is: per tile the tensor
+    // core sees
+    //   dK/dV: dV += P^T dO_t | S^T_{t+1} | dK += dS^T Q_t | dP^T_{t+1}
+    //   dQ:    S_{t+1} | dQ += dS K_t | dP_{t+1}
+    // Each product overwrites TMEM that an earlier one in this order reads
+    // (P^T over S^T, dS over dP), which the tensor pipe's in-order execution
+    // makes safe; the elementwise side has read those columns before it
+    // signals.
+    auto ring_wait = [&](int t) {
+      return wait_warp(ring_full(t % C::kRing), (t / C::kRing) & 1, ctl, kSiteMmaKV);
+    };
+    if (ok && (ok = ring_wait(0))) {
+      ptx::tc_fence_after();
+      issue_scores(tS, sFixed(0), sRing(0, 0));   // S^T = K Q_0^T  |  S = Q K_0^T
+      commit(s_full);
+      issue_scores(tP2, sFixed(1), sRing(0, 1));  // dP^T = V dO_0^T  |  dP = dO V_0^T
+      commit(dp_full);
+    }
     for (int t = 0; t < n_steps && ok; ++t) {
       const int slot = t % C::kRing;
-      if (!(ok = wait_warp(ring_full(slot), (t / C::kRing) & 1, ctl, kSiteMmaKV))) break;
-      ptx::tc_fence_after();
-      if constexpr (DKDV) {
-        issue_scores(tS, sFixed(0), sRing(slot, 0));   // S^T  = K  Q_i^T
-        issue_scores(tP2, sFixed(1), sRing(slot, 1));  // dP^T = V  dO_i^T
-      } else {
-        issue_scores(tS, sFixed(0), sRing(slot, 0));   // S  = Q  K_j^T
-        issue_scores(tP2, sFixed(1), sRing(slot, 1));  // dP = dO V_j^T
-      }
-      commit(s_full);
+      const int nslot = (t + 1) % C::kRing;
+      const bool more = t + 1 < n_steps;
       if (!(ok = wait_warp(p_ready, t & 1, ctl, kSiteMmaP))) break;
       ptx::tc_fence_after();
-      if constexpr (DKDV) {
-        issue_acc(tAcc0, tS, sRing(slot, 1), t == 0);   // dV += P^T  dO_i
-        issue_acc(tAcc1, tP2, sRing(slot, 0), t == 0);  // dK += dS^T Q_i
-      } else {
-        issue_acc(tAcc0, tS, sRing(slot, 0), t == 0);   // dQ += dS K_j
+      if constexpr (DKDV) issue_acc(tAcc0, tS, sRing(slot, 1), t == 0);  // dV += P^T dO_t
+      if (more) {
+        if (!(ok = ring_wait(t + 1))) break;
+        ptx::tc_fence_after();
+        issue_scores(tS, sFixed(0), sRing(nslot, 0));
+        commit(s_full);
       }
+      if (!(ok = wait_warp(ds_ready, t & 1, ctl, kSiteMmaP))) break;
+      ptx::tc_fence_after();
+      if constexpr (DKDV)
+        issue_acc(tAcc1, tP2, sRing(slot, 0), t == 0);  // dK += dS^T Q_t
+      else
+        issue_acc(tAcc0, tP2, sRing(slot, 0), t == 0);  // dQ += dS K_t
       commit(ring_empty(slot));
+      if (more) {
+        issue_scores(tP2, sFixed(1), sRing(nslot, 1));
+        commit(dp_full);
+      }
     }
     if (ok) commit(acc_full);
     // every MMA this warp issued completes before TMEM is released
@@ -332,51 +363,70 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      // four 32-column chunks; chunk k's bf16 results go to columns
-      // [16k, 16k + 16), all of which earlier loads have already read
-#pragma unroll 1
+      // P over this row's 128 columns, kept in registers for dS; in four
+      // 32-column chunks, chunk k's bf16 values go to columns [16k, 16k+16),
+      // which earlier loads have already read
+      float pr[128];
+#pragma unroll
       for (int k = 0; k < 4; ++k) {
-        uint32_t sr[32], dr[32];
+        uint32_t sr[32];
         ptx::tmem_ld_x32(tS + 32 * k, sr);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int c = 32 * k + i;
+          float lse2;
+          bool vis;
+          if constexpr (DKDV) {
+            lse2 = rowbuf[c].x;
+            vis = !CAUSAL || my <= y0 + c;  // key my, query y0 + c
+          } else {
+            lse2 = my_lse2;
+            const int key = y0 + c;
+            vis = key < N && (!CAUSAL || key <= my);
+          }
+          pr[c] = vis ? ptx::ex2(__uint_as_float(sr[i]) * sl2 - lse2) : 0.f;
+        }
+        if constexpr (DKDV) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(pr[32 * k + 2 * i], pr[32 * k + 2 * i + 1]);
+          ptx::tmem_st_x16(tS + 16 * k, pk);  // P^T over S^T
+        }
+      }
+      // dK/dV: P^T is in TMEM; dQ: S has been read.  Either way the issuer
+      // may go on (dV += P^T dO, or the next tile's scores over S).
+      if constexpr (DKDV) ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(p_ready);
+      if (!wait_warp(dp_full, t & 1, ctl, kSiteSoftmaxS)) {
+        ok = false;
+        break;
+      }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t dr[32];
         ptx::tmem_ld_x32(tP2 + 32 * k, dr);
-        uint32_t pk_p[16], pk_ds[16];
+        uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          float pp[2], dd[2];
+          float dd[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int c = 32 * k + 2 * i + e;
-            float lse2, dsum;
-            bool vis;
-            if constexpr (DKDV) {
-              const float2 ld = rowbuf[c];
-              lse2 = ld.x;
-              dsum = ld.y;
-              vis = !CAUSAL || my <= y0 + c;  // key my, query y0 + c
-            } else {
-              lse2 = my_lse2;
-              dsum = my_d;
-              const int key = y0 + c;
-              vis = key < N && (!CAUSAL || key <= my);
-            }
-            const float pe = vis ? ptx::ex2(__uint_as_float(sr[2 * i + e]) * sl2 - lse2) : 0.f;
-            pp[e] = pe;
-            dd[e] = pe * (__uint_as_float(dr[2 * i + e]) - dsum);
+            const float dsum = DKDV ? rowbuf[c].y : my_d;
+            dd[e] = pr[c] * (__uint_as_float(dr[2 * i + e]) - dsum);
           }
-          pk_p[i] = ptx::pack_bf16x2(pp[0], pp[1]);
-          pk_ds[i] = ptx::pack_bf16x2(dd[0], dd[1]);
+          pk[i] = ptx::pack_bf16x2(dd[0], dd[1]);
         }
-        if constexpr (DKDV) {
-          ptx::tmem_st_x16(tS + 16 * k, pk_p);    // P^T  over S^T
-          ptx::tmem_st_x16(tP2 + 16 * k, pk_ds);  // dS^T over dP^T
-        } else {
-          ptx::tmem_st_x16(tS + 16 * k, pk_ds);   // dS over S
-        }
+        // dS^T over dP^T (dK/dV) or dS over dP (dQ)
+        ptx::tmem_st_x16(tP2 + 16 * k, pk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(p_ready);
+      if (lane == 0) ptx::mbar_arrive(ds_ready);
     }
     if (ok && n_steps > 0 && wait_warp(acc_full, 0, ctl, kSiteSoftmaxO)) {
       ptx::tc_fence_after();

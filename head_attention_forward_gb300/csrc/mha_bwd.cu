@@ -48,7 +48,9 @@ cudaError_t launch_tile(const CUtensorMap& mq, const CUtensorMap& mk, const CUte
                         const CUtensorMap& mdo, const mha::BwdParams& prm, int BH,
                         cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(BH), static_cast<unsigned>(prm.n_tiles), 1);
+  cfg.gridDim = prm.tiles_fastest
+                    ? dim3(static_cast<unsigned>(prm.n_tiles), static_cast<unsigned>(BH), 1)
+                    : dim3(static_cast<unsigned>(BH), static_cast<unsigned>(prm.n_tiles), 1);
   cfg.blockDim = dim3(mha::BwdCfg<D>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = mha::BwdCfg<D>::kSmemBytes;
   cfg.stream = stream;
@@ -139,6 +141,9 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* o, const fl
   prm.wait_limit = wait_limit();
   prm.N = N;
   prm.n_tiles = (N + 127) / 128;
+  // 32+ tiles per head: one head's CTAs together (measured +5..8% at N >= 4096,
+  // -10% at N = 2048 causal); grid y is limited to 65535
+  prm.tiles_fastest = (prm.n_tiles >= 32 && BH <= 65535) ? 1 : 0;
   prm.scale = scale;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   cudaStream_t st = static_cast<cudaStream_t>(stream);

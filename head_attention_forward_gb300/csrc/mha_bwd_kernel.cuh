@@ -50,6 +50,7 @@ struct BwdParams {
   long long wait_limit;    // SM cycles per wait
   int N;
   int n_tiles;             // ceil(N / 128)
+  int tiles_fastest;       // grid is (n_tiles, BH) instead of (BH, n_tiles)
   float scale;             // score multiplier
   float scale_log2;        // scale * log2(e)
 };
@@ -137,12 +138,15 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
+  // Long sequences put a head's tiles next to each other in the launch
+  // order, so the CTAs of one head run together and share its tiles in L2;
+  // short ones keep heads fastest, which spreads the causal load better.
+  const int bh = p.tiles_fastest ? static_cast<int>(blockIdx.y) : static_cast<int>(blockIdx.x);
+  const int tpos = p.tiles_fastest ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y);
   const int N = p.N;
   // this CTA's own tile (keys for dK/dV, queries for dQ), heaviest first
   // under the causal mask
-  const int tile = (CAUSAL && !DKDV) ? (p.n_tiles - 1 - static_cast<int>(blockIdx.y))
-                                     : static_cast<int>(blockIdx.y);
+  const int tile = (CAUSAL && !DKDV) ? (p.n_tiles - 1 - tpos) : tpos;
   const int r0 = tile * C::kBlock;
   // the other side's tiles this CTA walks: [t_begin, t_end)
   const int t_begin = (CAUSAL && DKDV) ? tile : 0;
@@ -227,6 +231,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         for (int h = 0; h < C::kHalves; ++h) {
           ptx::tma_load_3d(sRing(slot, 0) + h * C::kHalfBytes, ring0, ring_full(slot), h * 64, y, bh);
           ptx::tma_load_3d(sRing(slot, 1) + h * C::kHalfBytes, ring1, ring_full(slot), h * 64, y, bh);
+        }
+        if (t + 2 < n_steps) {  // warm L2 two steps ahead (the ring holds two)
+          const int y2 = (t_begin + t + 2) * C::kBlock;
+          for (int h = 0; h < C::kHalves; ++h) {
+            ptx::tma_prefetch_3d(ring0, h * 64, y2, bh);
+            ptx::tma_prefetch_3d(ring1, h * 64, y2, bh);
+          }
         }
       }
       if (!ok) {

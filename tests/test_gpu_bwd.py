@@ -100,3 +100,13 @@ def test_bwd_long_sequence_two_heads():
     got = run_bwd(q, k, v, do, True)
     ref = oracle.attention_bwd(q, k, v, do, scale_for(128), True)
     check(got, ref, "N2048")
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_bwd_tiles_fastest_launch_order(causal):
+    """33 tiles per head (N = 4224, ragged): the launch order that keeps one
+    head's tiles together."""
+    q, k, v, do = inputs(13, 1, 2, 4224, 64)
+    got = run_bwd(q, k, v, do, causal)
+    ref = oracle.attention_bwd(q, k, v, do, scale_for(64), causal)
+    check(got, ref, f"N4224 causal={causal}")

@@ -108,3 +108,88 @@ def test_paged_equals_contiguous_when_identity():
                    ws, ws_bytes)
     torch.cuda.synchronize()
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def gather_or_zero(kc, table, b, n, page, num_blocks):
+    """Like gather(), but a block id outside [0, num_blocks) reads as zeros."""
+    H, d = kc.shape[1], kc.shape[3]
+    out = np.zeros((H, n, d), dtype=kc.dtype)
+    for t in range(n):
+        blk = table[b, t // page]
+        if 0 <= blk < num_blocks:
+            out[:, t] = kc[blk, :, t % page]
+    return out
+
+
+@pytest.mark.parametrize("page", [32, 256])
+def test_paged_odd_tables(page):
+    """Repeated block ids, ids outside the cache (read as zeros) and a length
+    beyond the table (clamped to max_blocks * page)."""
+    import torch
+
+    import head_attention_forward_gb300 as mha
+    B, H, Nq, d = 3, 2, 2, 128
+    max_blocks = 6
+    num_blocks = 8
+    rng = np.random.default_rng(page)
+    table = rng.integers(0, num_blocks, size=(B, max_blocks)).astype(np.int32)
+    table[0, 1] = table[0, 3]            # one physical block used twice
+    table[1, 2] = num_blocks + 5         # past the cache
+    table[1, 4] = -3                     # negative
+    seq = np.array([max_blocks * page - 5, 5 * page + 7, max_blocks * page + 100], dtype=np.int32)
+    kc = synth.normal_bf16(70 + page, synth.STREAM_K, num_blocks * H * page * d).reshape(num_blocks, H, page, d)
+    vc = synth.normal_bf16(70 + page, synth.STREAM_V, num_blocks * H * page * d).reshape(num_blocks, H, page, d)
+    q = synth.normal_bf16(70 + page, synth.STREAM_Q, B * H * Nq * d).reshape(B, H, Nq, d)
+    scale = scale_for(d)
+    o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, max_blocks * page, d, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    mha.mha_fwd_paged(to_device(q), to_device(kc), to_device(vc), torch.from_numpy(table).cuda(),
+                      torch.from_numpy(seq).cuda(), o, lse, B, H, Nq, d, page, num_blocks, max_blocks,
+                      scale, False, 0, ws, ws_bytes)
+    rc, word = mha.mha_device_status()
+    assert rc == mha.MHA_OK, f"status {word:#x}"
+    og, lg = bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    for b in range(B):
+        n = min(int(seq[b]), max_blocks * page)
+        kb = gather_or_zero(kc, table, b, n, page, num_blocks)
+        vb = gather_or_zero(vc, table, b, n, page, num_blocks)
+        o_ref, l_ref = oracle.attention_kv(q[b:b + 1], kb[None], vb[None], scale, False)
+        do = np.abs(og[b] - o_ref[0])
+        dl = np.abs(lg[b] - l_ref[0])
+        assert do.max() <= TOL_MAX_O and do.mean() <= TOL_MEAN_O and dl.max() <= TOL_MAX_LSE, \
+            (b, do.max(), do.mean(), dl.max())
+
+
+def test_paged_full_workload_sampled():
+    """The whole 32-sequence, 64-key-page decode workload in one call; a few
+    (sequence, head) rows checked against the oracle."""
+    import torch
+
+    import head_attention_forward_gb300 as mha
+    qb, kcb, vcb, table, seq = synth.paged_inputs("pag2")
+    c = synth.PAGED_CONFIGS["pag2"]
+    B, H, Nq, d, page = c["B"], c["H"], c["Nq"], c["d"], c["page"]
+    num_blocks, max_blocks = kcb.shape[0], table.shape[1]
+    scale = scale_for(d)
+    o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, max_blocks * page, d, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    mha.mha_fwd_paged(to_device(qb), to_device(kcb), to_device(vcb), torch.from_numpy(table).cuda(),
+                      torch.from_numpy(seq).cuda(), o, lse, B, H, Nq, d, page, num_blocks, max_blocks,
+                      scale, False, 0, ws, ws_bytes)
+    rc, word = mha.mha_device_status()
+    assert rc == mha.MHA_OK, f"status {word:#x}"
+    og, lg = bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    assert np.isfinite(og).all() and np.isfinite(lg).all()
+    for b in (0, 7, 31):
+        n = int(seq[b])
+        kb, vb = gather(kcb, table, b, n, page), gather(vcb, table, b, n, page)
+        for h in (0, 17, 31):
+            o_ref, l_ref = oracle.attention_kv(qb[b:b + 1, h:h + 1], kb[None, h:h + 1], vb[None, h:h + 1],
+                                               scale, False)
+            do = np.abs(og[b, h] - o_ref[0, 0])
+            dl = np.abs(lg[b, h] - l_ref[0, 0])
+            assert do.max() <= TOL_MAX_O and dl.max() <= TOL_MAX_LSE, (b, h, do.max(), dl.max())

@@ -33,6 +33,7 @@ struct DeviceState {
   bool ready = false;
   bool ok = false;
   unsigned* status = nullptr;
+  int sms = 0;  // multiprocessor count: the persistent grid's size
 };
 DeviceState g_dev[kMaxDevices];
 
@@ -85,6 +86,8 @@ int device_setup(int* dev_out, unsigned** status_out) {
                                  mha::FwdCfg<128>::kSmemBytes) != cudaSuccess;
     void* sym = nullptr;
     fail |= cudaGetSymbolAddress(&sym, g_status) != cudaSuccess;
+    fail |= cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            st.sms <= 0;
     if (fail) {
       st.ready = false;
       return MHA_ERR_CUDA;
@@ -96,6 +99,11 @@ int device_setup(int* dev_out, unsigned** status_out) {
   *dev_out = dev;
   *status_out = st.status;
   return MHA_OK;
+}
+
+int device_sms(int dev) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_dev[dev].sms;
 }
 
 bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows) {
@@ -145,11 +153,14 @@ long long wait_limit() {
 namespace {
 using namespace mha_host;
 
+// Persistent launch: one CTA per SM (fewer when there are fewer work tiles),
+// each walking its share of the (bh, m-block) tiles.
 template <int D, bool CAUSAL>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                   const mha::FwdParams& prm, int BH, cudaStream_t stream) {
+                   const mha::FwdParams& prm, int sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(BH), static_cast<unsigned>(prm.num_mblocks), 1);
+  const long long total = static_cast<long long>(prm.BH) * prm.num_mblocks;
+  cfg.gridDim = dim3(static_cast<unsigned>(total < sms ? total : sms), 1, 1);
   cfg.blockDim = dim3(mha::FwdCfg<D>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = mha::FwdCfg<D>::kSmemBytes;
   cfg.stream = stream;
@@ -212,15 +223,17 @@ int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   prm.wait_limit = wait_limit();
   prm.N = N;
   prm.num_mblocks = (N + 255) / 256;
+  prm.BH = static_cast<int>(BH);
+  const int sms = device_sms(dev);
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (d == 64)
-    err = causal ? launch<64, true>(mq, mk, mv, prm, static_cast<int>(BH), st)
-                 : launch<64, false>(mq, mk, mv, prm, static_cast<int>(BH), st);
+    err = causal ? launch<64, true>(mq, mk, mv, prm, sms, st)
+                 : launch<64, false>(mq, mk, mv, prm, sms, st);
   else
-    err = causal ? launch<128, true>(mq, mk, mv, prm, static_cast<int>(BH), st)
-                 : launch<128, false>(mq, mk, mv, prm, static_cast<int>(BH), st);
+    err = causal ? launch<128, true>(mq, mk, mv, prm, sms, st)
+                 : launch<128, false>(mq, mk, mv, prm, sms, st);
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 

@@ -9,12 +9,17 @@
 // l deferred to the end, and exp written as exp2 of a pre-scaled argument
 // (blog, Puzzle 8: exp(x) = 2^(log2(e) x)).
 //
-// How it maps to GB300 (one CTA = 256 query rows of one (batch, head)):
-//   warp 0      TMA producer: Q0/Q1 once, then K_j / V_j into a ring of
-//               shared-memory stages guarded by full/empty mbarriers (the
-//               producer/consumer tokens of the Triton warp-specialisation
-//               notes: acquire -> expect bytes -> TMA copy; consumer waits
-//               -> uses -> releases).
+// How it maps to GB300.  A work tile is 256 query rows of one (batch,
+// head), split into two 128-row Q tiles.  The kernel is persistent: one CTA
+// per SM walks its share of the work tiles, so TMEM, barriers and the K/V
+// ring are set up once and the next tile's loads overlap this one's tail.
+//   warp 0      TMA producer for K_j / V_j of every work tile in turn, into
+//               a ring of shared-memory stages guarded by full/empty
+//               mbarriers (the producer/consumer tokens of the Triton
+//               warp-specialisation notes: acquire -> expect bytes -> TMA
+//               copy; consumer waits -> uses -> releases).
+//   warp 2      TMA producer for Q0/Q1 of each work tile, as soon as the
+//               tensor core no longer reads the Q buffer set it reuses.
 //   warp 1      MMA issuer: S_j(s) = Q_s K_j^T with tcgen05.mma into
 //               TMEM, then O(s) += P_j(s) V_j with P read straight from
 //               TMEM.  The whole warp runs the issue loop (so descriptors and
@@ -25,7 +30,7 @@
 //               its S row from TMEM, masks, updates m and l, writes P (bf16)
 //               back over S, rescales O in TMEM when its max moved (the
 //               correction stage), and finally writes O / l and the LSE.
-//   warps 2-3   idle (keep the softmax warpgroups aligned to TMEM lanes).
+//   warp 3      idle (keeps the softmax warpgroups aligned to TMEM lanes).
 // The two Q tiles ping-pong: while one softmax warpgroup works on its S, the
 // tensor core runs the other tile's GEMMs (the cooperative M-split of the
 // warp-specialisation notes, one consumer group per half of the rows).
@@ -56,6 +61,7 @@ struct FwdParams {
   long long wait_limit;  // SM cycles per wait
   int N;
   int num_mblocks;     // ceil(N / 256)
+  int BH;              // batch * heads; work tiles are (bh, m-block) pairs
   float scale_log2;    // scale * log2(e)
 };
 
@@ -68,11 +74,13 @@ struct FwdCfg {
   static constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int kTileBytes = kHalves * kHalfBytes;
   static constexpr int kStages = (D == 128) ? 4 : 8;
+  // Q buffer sets: with two, the next work tile's Q loads during this one
+  static constexpr int kQSets = (D == 128) ? 1 : 2;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = 2 * kTileBytes;
+  static constexpr int kOffKV = kQSets * 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
-  // barriers: q_full[2] kv_full[S] kv_empty[S] s_full[2] p_ready[2] o_full[2] drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 2 + 2 + 2 + 1;
+  // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_ready[2] o_full[2] drain
+  static constexpr int kNumBars = 4 + 2 * kStages + 2 + 2 + 2 + 1;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
@@ -86,6 +94,14 @@ struct FwdCfg {
   static constexpr float kRescaleThreshold = 8.0f;
 };
 
+// Work tile u (0 <= u < BH * num_mblocks) is m-block r = u / BH of head
+// bh = u % BH, m-blocks heaviest first under the causal mask.  CTA c of G
+// takes tiles in rounds of G: round k gives it tile k*G + c, or k*G + G-1-c
+// on odd rounds, so the heavy and light ends of each round even out.
+__device__ __forceinline__ int fwd_tile_of_round(int k, int c, int G) {
+  return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     mha_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -98,29 +114,45 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int mblk = CAUSAL ? (p.num_mblocks - 1 - static_cast<int>(blockIdx.y))
-                          : static_cast<int>(blockIdx.y);
-  const int m0 = mblk * 256;
   const int N = p.N;
   const int n_tiles = (N + C::kBlockN - 1) / C::kBlockN;
+  const int total = p.BH * p.num_mblocks;
+  const int G = static_cast<int>(gridDim.x);
+  const int c = static_cast<int>(blockIdx.x);
   // K/V tiles each Q tile needs (0 when the Q tile lies past the end).
   auto tiles_for = [&](int row0) {
     return row0 >= N ? 0 : (CAUSAL ? min(n_tiles, row0 / C::kBlockN + 1) : n_tiles);
   };
-  const int n_s0 = tiles_for(m0), n_s1 = tiles_for(m0 + C::kBlockM);
-  auto n_s = [&](int s) { return s ? n_s1 : n_s0; };
-  const int n_kv = max(n_s0, n_s1);
+  // the k-th tile of this CTA: head, first query row, K/V tiles per stage
+  struct Tile {
+    int bh, m0, n0, n1;
+  };
+  auto tile_at = [&](int k, Tile& t) -> bool {
+    const int u = fwd_tile_of_round(k, c, G);
+    if (u >= total) return false;
+    t.bh = u % p.BH;
+    const int r = u / p.BH;
+    const int mblk = CAUSAL ? (p.num_mblocks - 1 - r) : r;
+    t.m0 = mblk * 256;
+    t.n0 = tiles_for(t.m0);
+    t.n1 = tiles_for(t.m0 + C::kBlockM);
+    return true;
+  };
 
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
-  auto q_full = [&](int s) { return bar(s); };
-  auto kv_full = [&](int i) { return bar(2 + i); };
-  auto kv_empty = [&](int i) { return bar(2 + C::kStages + i); };
-  auto s_full = [&](int s) { return bar(2 + 2 * C::kStages + s); };
-  auto p_ready = [&](int s) { return bar(4 + 2 * C::kStages + s); };
-  auto o_full = [&](int s) { return bar(6 + 2 * C::kStages + s); };
-  const uint32_t drain_bar = bar(8 + 2 * C::kStages);
-  auto sQ = [&](int s) -> uint32_t { return sbase + C::kOffQ + s * C::kTileBytes; };
+  // Q set b holds work tiles b, b + kQSets, ...: the m-th use of a set is
+  // phase m of its barriers
+  auto q_full = [&](int b) { return bar(b); };       // both stages' Q tiles loaded
+  auto q_empty = [&](int b) { return bar(2 + b); };  // every S MMA reading them done
+  auto q_set = [](int k) { return k % C::kQSets; };
+  auto q_par = [](int k) { return (k / C::kQSets) & 1; };
+  auto kv_full = [&](int i) { return bar(4 + i); };
+  auto kv_empty = [&](int i) { return bar(4 + C::kStages + i); };
+  auto s_full = [&](int s) { return bar(4 + 2 * C::kStages + s); };
+  auto p_ready = [&](int s) { return bar(6 + 2 * C::kStages + s); };
+  auto o_full = [&](int s) { return bar(8 + 2 * C::kStages + s); };
+  const uint32_t drain_bar = bar(10 + 2 * C::kStages);
+  auto sQ = [&](int b, int s) -> uint32_t { return sbase + C::kOffQ + (2 * b + s) * C::kTileBytes; };
   auto sKV = [&](int i) -> uint32_t { return sbase + C::kOffKV + i * C::kTileBytes; };
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
@@ -128,8 +160,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit};
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(q_full(0), 1);
-    ptx::mbar_init(q_full(1), 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(q_full(b), 1);
+      ptx::mbar_init(q_empty(b), 1);
+    }
     for (int i = 0; i < C::kStages; ++i) {
       ptx::mbar_init(kv_full(i), 1);
       ptx::mbar_init(kv_empty(i), 1);
@@ -158,39 +192,64 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // -------------------------------------------------- K/V producer
+    // K_j, V_j of every work tile in turn through one ring; position t
+    // runs on across work tiles.
     if (lane == 0) {
-      for (int s = 0; s < 2; ++s) {
-        if (n_s(s) == 0) continue;
-        ptx::mbar_arrive_expect_tx(q_full(s), C::kTileBytes);
-        for (int h = 0; h < C::kHalves; ++h)
-          ptx::tma_load_3d(sQ(s) + h * C::kHalfBytes, &tmQ, q_full(s), h * 64,
-                           m0 + s * C::kBlockM, bh);
-      }
-      int t = 0;  // ring position: K_j is load 2j, V_j is load 2j + 1
+      int t = 0;
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        for (int which = 0; which < 2; ++which, ++t) {
-          const int slot = t % C::kStages;
-          const int use = t / C::kStages;
-          if (use > 0 && !wait_one(kv_empty(slot), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
-            ok = false;
-            break;
+      Tile tl;
+      for (int k = 0; ok && tile_at(k, tl); ++k) {
+        const int n_kv = max(tl.n0, tl.n1);
+        for (int j = 0; j < n_kv && ok; ++j) {
+          for (int which = 0; which < 2; ++which, ++t) {
+            const int slot = t % C::kStages;
+            const int use = t / C::kStages;
+            if (use > 0 && !wait_one(kv_empty(slot), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
+            const CUtensorMap* map = which ? &tmV : &tmK;
+            for (int h = 0; h < C::kHalves; ++h)
+              ptx::tma_load_3d(sKV(slot) + h * C::kHalfBytes, map, kv_full(slot), h * 64,
+                               j * C::kBlockN, tl.bh);
           }
-          ptx::mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
-          const CUtensorMap* map = which ? &tmV : &tmK;
-          for (int h = 0; h < C::kHalves; ++h)
-            ptx::tma_load_3d(sKV(slot) + h * C::kHalfBytes, map, kv_full(slot), h * 64,
-                             j * C::kBlockN, bh);
         }
       }
       if (!ok) {
         // let the copies already issued land before the CTA goes away
-        for (int s = 0; s < 2; ++s)
-          if (n_s(s) > 0) drain_wait(q_full(s), 0, ctl);
         for (int u = max(0, t - C::kStages); u < t; ++u)
           drain_wait(kv_full(u % C::kStages), (u / C::kStages) & 1, ctl);
       }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------ Q producer
+    // The next work tile's Q goes in as soon as the tensor core has run the
+    // current tile's last Q K^T, overlapping that tile's last softmax and
+    // epilogue.
+    if (lane == 0) {
+      Tile tl;
+      int k = 0;
+      bool ok = true;
+      for (; ok && tile_at(k, tl); ++k) {
+        // the set's previous tile (k - kQSets) must be done with it
+        const int prev = k - C::kQSets;
+        if (prev >= 0 && !wait_one(q_empty(q_set(prev)), q_par(prev), ctl, kSiteProducerEmpty)) {
+          ok = false;
+          break;
+        }
+        const int b = q_set(k);
+        const int stages = tl.n1 > 0 ? 2 : 1;
+        ptx::mbar_arrive_expect_tx(q_full(b), stages * C::kTileBytes);
+        for (int s = 0; s < stages; ++s)
+          for (int h = 0; h < C::kHalves; ++h)
+            ptx::tma_load_3d(sQ(b, s) + h * C::kHalfBytes, &tmQ, q_full(b), h * 64,
+                             tl.m0 + s * C::kBlockM, tl.bh);
+      }
+      if (!ok)
+        for (int u = max(0, k - C::kQSets); u < k; ++u) drain_wait(q_full(q_set(u)), q_par(u), ctl);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -208,7 +267,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // Every lane of the warp runs this loop with the same values; that
       // keeps them warp-uniform, and an elected lane issues.
       // Q and K tiles: K-major, 128-byte swizzle, 8-row groups 1 KiB apart.
-      const uint64_t dQ0 = ptx::desc_sw128(sQ(0), 16, 1024), dQ1 = ptx::desc_sw128(sQ(1), 16, 1024);
+      const uint64_t dQ00 = ptx::desc_sw128(sQ(0, 0), 16, 1024);
       const uint64_t dK0 = ptx::desc_sw128(sKV(0), 16, 1024);
       // V tiles: MN-major (d contiguous), d-halves 16 KiB apart (LBO),
       // 8-key groups 1 KiB apart (SBO).
@@ -217,9 +276,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         return static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
       };
       // S(s) = Q_s K^T over K = d in steps of 16
-      auto issue_s = [&](int s, int kslot) {
+      auto issue_s = [&](int qb, int s, int kslot) {
         const uint64_t dk = dK0 + slot_off(kslot);
-        const uint64_t dq = s ? dQ1 : dQ0;
+        const uint64_t dq = dQ00 + static_cast<uint64_t>(((2 * qb + s) * C::kTileBytes) >> 4);
         const uint32_t ts = s ? tS1 : tS0;
         if (ptx::elect_one()) {
 #pragma unroll
@@ -249,52 +308,47 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         __syncwarp();
       };
       bool ok = true;
-      for (int s = 0; s < 2 && ok; ++s)
-        if (n_s(s) > 0) ok = wait_warp(q_full(s), 0, ctl, kSiteMmaQ);
-      int t = 0;
-      int v_prev = 0;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int k_slot = t % C::kStages, k_par = (t / C::kStages) & 1;
-        ++t;
-        const int v_slot = t % C::kStages, v_par = (t / C::kStages) & 1;
-        ++t;
-        if (!wait_warp(kv_full(k_slot), k_par, ctl, kSiteMmaKV)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        for (int s = 0; s < 2 && ok; ++s) {
-          if (j >= 1 && j - 1 < n_s(s)) {
-            if (!wait_warp(p_ready(s), (j - 1) & 1, ctl, kSiteMmaP)) {
-              ok = false;
-              break;
+      int t = 0;                 // K/V ring position
+      int pr[2] = {0, 0};        // p_ready completions consumed, per stage
+      Tile tl;
+      for (int k = 0; ok && tile_at(k, tl); ++k) {
+        auto n_s = [&](int s) { return s ? tl.n1 : tl.n0; };
+        const int n_kv = max(tl.n0, tl.n1);
+        const int qb = q_set(k);
+        if (!(ok = wait_warp(q_full(qb), q_par(k), ctl, kSiteMmaQ))) break;
+        int v_prev = 0;
+        for (int j = 0; j < n_kv && ok; ++j) {
+          const int k_slot = t % C::kStages, k_par = (t / C::kStages) & 1;
+          ++t;
+          const int v_slot = t % C::kStages, v_par = (t / C::kStages) & 1;
+          ++t;
+          if (!(ok = wait_warp(kv_full(k_slot), k_par, ctl, kSiteMmaKV))) break;
+          ptx::tc_fence_after();
+          for (int s = 0; s < 2 && ok; ++s) {
+            if (j >= 1 && j - 1 < n_s(s)) {
+              if (!(ok = wait_warp(p_ready(s), pr[s] & 1, ctl, kSiteMmaP))) break;
+              ++pr[s];
+              ptx::tc_fence_after();
+              issue_pv(s, v_prev, j - 1 == 0);
+              if (j - 1 == n_s(s) - 1) commit(o_full(s));
             }
-            ptx::tc_fence_after();
-            issue_pv(s, v_prev, j - 1 == 0);
-            if (j - 1 == n_s(s) - 1) commit(o_full(s));
+            if (j < n_s(s)) {
+              issue_s(qb, s, k_slot);
+              commit(s_full(s));
+            }
           }
-          if (j < n_s(s)) {
-            issue_s(s, k_slot);
-            commit(s_full(s));
-          }
+          if (!ok) break;
+          if (j == n_kv - 1) commit(q_empty(qb));  // this tile's Q is no longer read
+          commit(kv_empty(k_slot));
+          if (j >= 1) commit(kv_empty(v_prev));
+          if (!(ok = wait_warp(kv_full(v_slot), v_par, ctl, kSiteMmaKV))) break;
+          ptx::tc_fence_after();
+          v_prev = v_slot;
         }
-        if (!ok) break;
-        commit(kv_empty(k_slot));
-        if (j >= 1) commit(kv_empty(v_prev));
-        if (!wait_warp(kv_full(v_slot), v_par, ctl, kSiteMmaKV)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        v_prev = v_slot;
-      }
-      if (ok) {
         for (int s = 0; s < 2 && ok; ++s) {
           if (n_kv - 1 < n_s(s)) {
-            if (!wait_warp(p_ready(s), (n_kv - 1) & 1, ctl, kSiteMmaP)) {
-              ok = false;
-              break;
-            }
+            if (!(ok = wait_warp(p_ready(s), pr[s] & 1, ctl, kSiteMmaP))) break;
+            ++pr[s];
             ptx::tc_fence_after();
             issue_pv(s, v_prev, n_kv - 1 == 0);
             commit(o_full(s));
@@ -312,118 +366,130 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const int s = (warp - 4) >> 2;
     const int wq = warp & 3;  // TMEM lane quarter this warp may access
     const int row = wq * 32 + lane;
-    const int q_idx = m0 + s * C::kBlockM + row;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
     const uint32_t t_s = tmem + lane_off + (s ? C::kColS1 : C::kColS0);
     const uint32_t t_o = tmem + lane_off + (s ? C::kColO1 : C::kColO0);
     const float sl2 = p.scale_log2;
-    const int n = n_s(s);
-    float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale
-    float l_run = 0.f;   // row sum of exp2 terms (fp32), for the LSE
-    float lr_run = 0.f;  // the same over the bf16-rounded terms, for O
     bool ok = true;
-    for (int j = 0; j < n; ++j) {
-      if (!wait_warp(s_full(s), j & 1, ctl, kSiteSoftmaxS)) {
+    int sf = 0;  // s_full completions consumed
+    int of = 0;  // o_full completions consumed
+    Tile tl;
+    for (int k = 0; ok && tile_at(k, tl); ++k) {
+      const int m0 = tl.m0;
+      const int n = s ? tl.n1 : tl.n0;
+      const int q_idx = m0 + s * C::kBlockM + row;
+      float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale
+      float l_run = 0.f;   // row sum of exp2 terms (fp32), for the LSE
+      float lr_run = 0.f;  // the same over the bf16-rounded terms, for O
+      for (int j = 0; j < n; ++j) {
+        if (!wait_warp(s_full(s), sf & 1, ctl, kSiteSoftmaxS)) {
+          ok = false;
+          break;
+        }
+        ++sf;
+        ptx::tc_fence_after();
+        uint32_t raw[128];
+        ptx::tmem_ld_x128(t_s, raw);
+        float x[128];
+#pragma unroll
+        for (int cc = 0; cc < 128; ++cc) x[cc] = __uint_as_float(raw[cc]);
+        const int kv0 = j * C::kBlockN;
+        const bool edge = (kv0 + C::kBlockN > N) || (CAUSAL && kv0 + C::kBlockN - 1 > m0 + s * C::kBlockM);
+        if (edge) {
+          const int lim = (CAUSAL ? min(N, q_idx + 1) : N) - kv0;  // keys [kv0, kv0+lim) visible
+#pragma unroll
+          for (int cc = 0; cc < 128; ++cc)
+            if (cc >= lim) x[cc] = -INFINITY;
+        }
+        // row maximum of this tile: 8 independent chains of 3-input max
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = x[i];
+#pragma unroll
+        for (int cc = 8; cc < 128; cc += 2) mx[(cc >> 1) & 7] = ptx::max3(mx[(cc >> 1) & 7], x[cc], x[cc + 1]);
+        const float tile_max = fmaxf(ptx::max3(mx[0], mx[1], mx[2]),
+                                     fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_tile = tile_max * sl2;
+        float alpha = 1.f;
+        if (m_tile > m_run + C::kRescaleThreshold) {
+          alpha = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - m_tile);
+          m_run = m_tile;
+        }
+        const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
+        const float2 sl2v = make_float2(sl2, sl2);
+        const float2 negm = make_float2(neg_m, neg_m);
+        float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // fp32 p: for the LSE
+        float sumr[4] = {0.f, 0.f, 0.f, 0.f};  // bf16 p: for O / l
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float2 tt = __ffma2_rn(make_float2(x[c4 * 32 + 2 * i], x[c4 * 32 + 2 * i + 1]), sl2v, negm);
+            const float p0 = ptx::ex2(tt.x);
+            const float p1 = ptx::ex2(tt.y);
+            pk[i] = ptx::pack_bf16x2(p0, p1);
+            sum2[i & 1] = __fadd2_rn(sum2[i & 1], make_float2(p0, p1));
+            // normalising O by the sum of the bf16 values the tensor core
+            // multiplies into V keeps O an exact convex combination of V rows
+            sumr[(2 * i) & 3] = ptx::add_bf16_lo(pk[i], sumr[(2 * i) & 3]);
+            sumr[(2 * i + 1) & 3] = ptx::add_bf16_hi(pk[i], sumr[(2 * i + 1) & 3]);
+          }
+          ptx::tmem_st_x16(t_s + c4 * 16, pk);
+        }
+        l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
+        lr_run = lr_run * alpha + ((sumr[0] + sumr[1]) + (sumr[2] + sumr[3]));
+        // correction: bring O(s) to the new max before P_j(s) V_j lands on it
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t ov[32];
+            ptx::tmem_ld_x32(t_o + cc * 32, ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            ptx::tmem_st_x32(t_o + cc * 32, ov);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(p_ready(s));
+      }
+      if (!ok || n == 0) continue;
+      if (!wait_warp(o_full(s), of & 1, ctl, kSiteSoftmaxO)) {
         ok = false;
         break;
       }
+      ++of;
       ptx::tc_fence_after();
-      uint32_t raw[128];
-      ptx::tmem_ld_x128(t_s, raw);
-      float x[128];
+      // epilogue: O = O_acc / l in bf16, LSE = (m + log2 l) * ln 2.  The next
+      // work tile's first P V overwrites O(s) only after this warp's next
+      // p_ready arrival, which follows these reads.
+      const bool valid = q_idx < N;
+      const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
+      __nv_bfloat16* orow = p.o + (static_cast<size_t>(tl.bh) * N + (valid ? q_idx : 0)) * D;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(raw[c]);
-      const int kv0 = j * C::kBlockN;
-      const bool edge = (kv0 + C::kBlockN > N) || (CAUSAL && kv0 + C::kBlockN - 1 > m0 + s * C::kBlockM);
-      if (edge) {
-        const int lim = (CAUSAL ? min(N, q_idx + 1) : N) - kv0;  // keys [kv0, kv0+lim) visible
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) x[c] = -INFINITY;
-      }
-      // row maximum of this tile: 8 independent chains of 3-input max
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = x[i];
-#pragma unroll
-      for (int c = 8; c < 128; c += 2) mx[(c >> 1) & 7] = ptx::max3(mx[(c >> 1) & 7], x[c], x[c + 1]);
-      const float tile_max = fmaxf(ptx::max3(mx[0], mx[1], mx[2]),
-                                   fmaxf(ptx::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_tile = tile_max * sl2;
-      float alpha = 1.f;
-      if (m_tile > m_run + C::kRescaleThreshold) {
-        alpha = (m_run == -INFINITY) ? 0.f : ptx::ex2(m_run - m_tile);
-        m_run = m_tile;
-      }
-      const float neg_m = (m_run == -INFINITY) ? 0.f : -m_run;
-      const float2 sl2v = make_float2(sl2, sl2);
-      const float2 negm = make_float2(neg_m, neg_m);
-      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // fp32 p: for the LSE
-      float sumr[4] = {0.f, 0.f, 0.f, 0.f};  // bf16 p: for O / l
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t ov[32];
+        ptx::tmem_ld_x32(t_o + cc * 32, ov);
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 t = __ffma2_rn(make_float2(x[c4 * 32 + 2 * i], x[c4 * 32 + 2 * i + 1]), sl2v, negm);
-          const float p0 = ptx::ex2(t.x);
-          const float p1 = ptx::ex2(t.y);
-          pk[i] = ptx::pack_bf16x2(p0, p1);
-          sum2[i & 1] = __fadd2_rn(sum2[i & 1], make_float2(p0, p1));
-          // normalising O by the sum of the bf16 values the tensor core
-          // multiplies into V keeps O an exact convex combination of V rows
-          sumr[(2 * i) & 3] = ptx::add_bf16_lo(pk[i], sumr[(2 * i) & 3]);
-          sumr[(2 * i + 1) & 3] = ptx::add_bf16_hi(pk[i], sumr[(2 * i + 1) & 3]);
-        }
-        ptx::tmem_st_x16(t_s + c4 * 16, pk);
-      }
-      l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
-      lr_run = lr_run * alpha + ((sumr[0] + sumr[1]) + (sumr[2] + sumr[3]));
-      // correction: bring O(s) to the new max before P_j(s) V_j lands on it
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          ptx::tmem_ld_x32(t_o + c * 32, ov);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          ptx::tmem_st_x32(t_o + c * 32, ov);
-        }
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(p_ready(s));
-    }
-    if (ok && n > 0) {
-      if (wait_warp(o_full(s), 0, ctl, kSiteSoftmaxO)) {
-        ptx::tc_fence_after();
-        // epilogue: O = O_acc / l in bf16, LSE = (m + log2 l) * ln 2
-        const bool valid = q_idx < N;
-        const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
-        __nv_bfloat16* orow = p.o + (static_cast<size_t>(bh) * N + (valid ? q_idx : 0)) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          ptx::tmem_ld_x32(t_o + c * 32, ov);
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
-                                     __uint_as_float(ov[2 * i + 1]) * inv_l);
-          if (valid) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4)
-              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
-          }
-        }
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                   __uint_as_float(ov[2 * i + 1]) * inv_l);
         if (valid) {
-          const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
-          p.lse[static_cast<size_t>(bh) * N + q_idx] =
-              l_run > 0.f ? (m_fin + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4)
+            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
+      if (valid) {
+        const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
+        p.lse[static_cast<size_t>(tl.bh) * N + q_idx] =
+            l_run > 0.f ? (m_fin + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+      }
+      ptx::tc_fence_before();
     }
   }
 

@@ -11,6 +11,9 @@ namespace mha_host {
 // word address.  Returns an mha_status code; on success fills dev / status.
 int device_setup(int* dev, unsigned** status);
 
+// Multiprocessor count of a device device_setup has accepted.
+int device_sms(int dev);
+
 // 3-D TMA view [BH][N][d] of a contiguous bf16 tensor, box 64 x box_rows x 1,
 // 128-byte swizzle; rows past N read as zero.
 bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int box_rows);

@@ -369,6 +369,11 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         }
         __syncwarp();
       }
+      // only a tile on the causal diagonal, or (dQ) one holding keys past
+      // N, needs a per-element mask; queries past N (dK/dV) get P = 0 from
+      // their LSE of +inf
+      const bool edge = DKDV ? (CAUSAL && y0 < r0 + C::kBlock)
+                             : (y0 + C::kBlock > N || (CAUSAL && y0 + C::kBlock - 1 > r0));
       if (!wait_warp(s_full, t & 1, ctl, kSiteSoftmaxS)) {
         ok = false;
         break;
@@ -385,17 +390,22 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int c = 32 * k + i;
-          float lse2;
-          bool vis;
-          if constexpr (DKDV) {
-            lse2 = rowbuf[c].x;
-            vis = !CAUSAL || my <= y0 + c;  // key my, query y0 + c
-          } else {
-            lse2 = my_lse2;
-            const int key = y0 + c;
-            vis = key < N && (!CAUSAL || key <= my);
+          const float lse2 = DKDV ? rowbuf[c].x : my_lse2;
+          pr[c] = ptx::ex2(__uint_as_float(sr[i]) * sl2 - lse2);
+        }
+        if (edge) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = 32 * k + i;
+            bool vis;
+            if constexpr (DKDV) {
+              vis = !CAUSAL || my <= y0 + c;  // key my, query y0 + c
+            } else {
+              const int key = y0 + c;
+              vis = key < N && (!CAUSAL || key <= my);
+            }
+            pr[c] = vis ? pr[c] : 0.f;
           }
-          pr[c] = vis ? ptx::ex2(__uint_as_float(sr[i]) * sl2 - lse2) : 0.f;
         }
         if constexpr (DKDV) {
           uint32_t pk[16];

@@ -66,7 +66,7 @@ struct BwdCfg {
   // fixed pair (K,V for dK/dV; Q,dO for dQ), then the ring of pairs
   static constexpr int kOffFixed = 0;
   static constexpr int kOffRing = 2 * kTileBytes;
-  static constexpr int kOffRowBuf = kOffRing + kRing * 2 * kTileBytes;  // float2 [4 warps][128]
+  static constexpr int kOffRowBuf = kOffRing + kRing * 2 * kTileBytes;  // float [4 warps][2][128]
   static constexpr int kOffBar = kOffRowBuf + 4 * 128 * 8;
   // barriers: fixed_full ring_full[R] ring_empty[R] s_full dp_full p_ready
   //           ds_ready acc_full drain
@@ -347,8 +347,10 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const float sl2 = p.scale_log2;
     constexpr float kLog2e = 1.4426950408889634f;
     const size_t base = static_cast<size_t>(bh) * N;
-    // per-warp copy of the current query tile's (LSE * log2 e, D) (dK/dV)
-    float2* rowbuf = reinterpret_cast<float2*>(smem + C::kOffRowBuf) + (warp - 4) * 128;
+    // per-warp copy of the current query tile's LSE * log2 e and D (dK/dV),
+    // as two float[128] arrays so one 16-byte load covers four columns
+    float* lse_buf = reinterpret_cast<float*>(smem + C::kOffRowBuf) + (warp - 4) * 256;
+    float* d_buf = lse_buf + 128;
     // this row's own (LSE * log2 e, D) (dQ); rows past N see no key
     float my_lse2 = INFINITY, my_d = 0.f;
     if (!DKDV && my < N) {
@@ -364,8 +366,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           const int c = lane + 32 * m;
           const int qi = y0 + c;
           // a query past N has LSE = +inf here, so its P and dS are 0
-          rowbuf[c] = qi < N ? make_float2(p.lse[base + qi] * kLog2e, p.dsum[base + qi])
-                             : make_float2(INFINITY, 0.f);
+          lse_buf[c] = qi < N ? p.lse[base + qi] * kLog2e : INFINITY;
+          d_buf[c] = qi < N ? p.dsum[base + qi] : 0.f;
         }
         __syncwarp();
       }
@@ -388,10 +390,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         uint32_t sr[32];
         ptx::tmem_ld_x32(tS + 32 * k, sr);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = 32 * k + i;
-          const float lse2 = DKDV ? rowbuf[c].x : my_lse2;
-          pr[c] = ptx::ex2(__uint_as_float(sr[i]) * sl2 - lse2);
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const int c = 32 * k + 4 * i4;
+          const float4 l4 = DKDV ? *reinterpret_cast<const float4*>(lse_buf + c)
+                                 : make_float4(my_lse2, my_lse2, my_lse2, my_lse2);
+          pr[c] = ptx::ex2(__uint_as_float(sr[4 * i4]) * sl2 - l4.x);
+          pr[c + 1] = ptx::ex2(__uint_as_float(sr[4 * i4 + 1]) * sl2 - l4.y);
+          pr[c + 2] = ptx::ex2(__uint_as_float(sr[4 * i4 + 2]) * sl2 - l4.z);
+          pr[c + 3] = ptx::ex2(__uint_as_float(sr[4 * i4 + 3]) * sl2 - l4.w);
         }
         if (edge) {
 #pragma unroll
@@ -431,15 +437,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         ptx::tmem_ld_x32(tP2 + 32 * k, dr);
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float dd[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int c = 32 * k + 2 * i + e;
-            const float dsum = DKDV ? rowbuf[c].y : my_d;
-            dd[e] = pr[c] * (__uint_as_float(dr[2 * i + e]) - dsum);
-          }
-          pk[i] = ptx::pack_bf16x2(dd[0], dd[1]);
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const int c = 32 * k + 4 * i4;
+          const float4 d4 = DKDV ? *reinterpret_cast<const float4*>(d_buf + c)
+                                 : make_float4(my_d, my_d, my_d, my_d);
+          pk[2 * i4] = ptx::pack_bf16x2(pr[c] * (__uint_as_float(dr[4 * i4]) - d4.x),
+                                        pr[c + 1] * (__uint_as_float(dr[4 * i4 + 1]) - d4.y));
+          pk[2 * i4 + 1] = ptx::pack_bf16x2(pr[c + 2] * (__uint_as_float(dr[4 * i4 + 2]) - d4.z),
+                                            pr[c + 3] * (__uint_as_float(dr[4 * i4 + 3]) - d4.w));
         }
         // dS^T over dP^T (dK/dV) or dS over dP (dQ)
         ptx::tmem_st_x16(tP2 + 16 * k, pk);

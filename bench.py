@@ -314,7 +314,9 @@ def run_decode(args, name):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": gbs / hbm_peak, "traffic": recorded_traffic(name),
                      "algorithmic_bytes_per_step": algo_bytes,
-                     "kernel": f"splitkv_partial_kernel<{d}> + splitkv_merge_kernel<{d}>"},
+                     "kernel": (f"mha_fwd_kernel<{d},{int(bool(causal))},split> + splitkv_merge_kernel<{d}>"
+                                if (d == 128 or Nq >= 3) else  # the library's choice of partial pass
+                                f"splitkv_partial_kernel<{d}> + splitkv_merge_kernel<{d}>")},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }

@@ -72,18 +72,18 @@ int device_setup(int* dev_out, unsigned** status_out) {
       g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     bool fail = false;
-    fail |= cudaFuncSetAttribute(mha::mha_fwd_kernel<64, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 mha::FwdCfg<64>::kSmemBytes) != cudaSuccess;
-    fail |= cudaFuncSetAttribute(mha::mha_fwd_kernel<64, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 mha::FwdCfg<64>::kSmemBytes) != cudaSuccess;
-    fail |= cudaFuncSetAttribute(mha::mha_fwd_kernel<128, false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 mha::FwdCfg<128>::kSmemBytes) != cudaSuccess;
-    fail |= cudaFuncSetAttribute(mha::mha_fwd_kernel<128, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 mha::FwdCfg<128>::kSmemBytes) != cudaSuccess;
+    auto smem_attr = [&](auto kernel, int bytes) {
+      fail |= cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+              cudaSuccess;
+    };
+    smem_attr(mha::mha_fwd_kernel<64, false, false>, mha::FwdCfg<64>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, true, false>, mha::FwdCfg<64>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, false, false>, mha::FwdCfg<128>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, true, false>, mha::FwdCfg<128>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, false, true>, mha::FwdCfg<64>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, true, true>, mha::FwdCfg<64>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, false, true>, mha::FwdCfg<128>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, true, true>, mha::FwdCfg<128>::kSmemBytes);
     void* sym = nullptr;
     fail |= cudaGetSymbolAddress(&sym, g_status) != cudaSuccess;
     fail |= cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -151,22 +151,63 @@ long long wait_limit() {
 }  // namespace mha_host
 
 namespace {
+template <int D, bool CAUSAL, bool SPLIT>
+cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                   const mha::FwdParams& prm, int sms, cudaStream_t stream);
+}  // namespace
+
+namespace mha_host {
+
+int fwd_split_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                      int BH, int Nq, int Nk, int d, float scale, bool causal, int num_splits,
+                      int tiles_per_split, int dev, unsigned* status, cudaStream_t st) {
+  CUtensorMap mq, mk, mv;
+  if (!encode_map(&mq, q, BH, Nq, d, 128) || !encode_map(&mk, k, BH, Nk, d, 128) ||
+      !encode_map(&mv, v, BH, Nk, d, 128))
+    return MHA_ERR_CUDA;
+  mha::FwdParams prm = {};
+  prm.status = status;
+  prm.wait_limit = wait_limit();
+  prm.N = Nk;
+  prm.num_mblocks = 1;
+  prm.BH = BH;
+  prm.Nq = Nq;
+  prm.Nk = Nk;
+  prm.num_splits = num_splits;
+  prm.tiles_per_split = tiles_per_split;
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  const int sms = device_sms(dev);
+  cudaError_t err;
+  if (d == 64)
+    err = causal ? launch<64, true, true>(mq, mk, mv, prm, sms, st)
+                 : launch<64, false, true>(mq, mk, mv, prm, sms, st);
+  else
+    err = causal ? launch<128, true, true>(mq, mk, mv, prm, sms, st)
+                 : launch<128, false, true>(mq, mk, mv, prm, sms, st);
+  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+}  // namespace mha_host
+
+namespace {
 using namespace mha_host;
 
 // Persistent launch: one CTA per SM (fewer when there are fewer work tiles),
-// each walking its share of the (bh, m-block) tiles.
-template <int D, bool CAUSAL>
+// each walking its share of the (bh, m-block) or (bh, split) tiles.
+template <int D, bool CAUSAL, bool SPLIT = false>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                    const mha::FwdParams& prm, int sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  const long long total = static_cast<long long>(prm.BH) * prm.num_mblocks;
+  const long long total = static_cast<long long>(prm.BH) * (SPLIT ? prm.num_splits : prm.num_mblocks);
   cfg.gridDim = dim3(static_cast<unsigned>(total < sms ? total : sms), 1, 1);
   cfg.blockDim = dim3(mha::FwdCfg<D>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = mha::FwdCfg<D>::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, mha::mha_fwd_kernel<D, CAUSAL>, mq, mk, mv, prm);
+  return cudaLaunchKernelEx(&cfg, mha::mha_fwd_kernel<D, CAUSAL, SPLIT>, mq, mk, mv, prm);
 }
 
 }  // namespace

@@ -62,6 +62,13 @@ struct FwdParams {
   int N;
   int num_mblocks;     // ceil(N / 256)
   int BH;              // batch * heads; work tiles are (bh, m-block) pairs
+  // split mode only: Nq queries per head (one Q tile, rows past Nq read as
+  // zeros) against Nk keys cut into num_splits runs of tiles_per_split
+  // K/V tiles; work tiles are (bh, split) pairs and each writes an fp32
+  // partial output normalised by its own sum, plus its log-sum-exp
+  int Nq, Nk, num_splits, tiles_per_split;
+  float* o_part;       // [BH, num_splits, Nq, D]
+  float* lse_part;     // [BH, num_splits, Nq]
   float scale_log2;    // scale * log2(e)
 };
 
@@ -102,7 +109,10 @@ __device__ __forceinline__ int fwd_tile_of_round(int k, int c, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
-template <int D, bool CAUSAL>
+// SPLIT = false: the attention forward pass (square, top-left causal mask).
+// SPLIT = true: the partial pass of split-KV decoding (bottom-right causal
+// mask, fp32 partial outputs for splitkv_merge_kernel); only stage 0 is used.
+template <int D, bool CAUSAL, bool SPLIT = false>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     mha_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -114,9 +124,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = p.N;
+  const int N = SPLIT ? p.Nk : p.N;  // keys (and, square, queries)
   const int n_tiles = (N + C::kBlockN - 1) / C::kBlockN;
-  const int total = p.BH * p.num_mblocks;
+  const int total = p.BH * (SPLIT ? p.num_splits : p.num_mblocks);
   const int G = static_cast<int>(gridDim.x);
   const int c = static_cast<int>(blockIdx.x);
   // K/V tiles each Q tile needs (0 when the Q tile lies past the end).
@@ -125,12 +135,22 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   };
   // the k-th tile of this CTA: head, first query row, K/V tiles per stage
   struct Tile {
-    int bh, m0, n0, n1;
+    int bh, m0, n0, n1, kv_begin, split;
   };
   auto tile_at = [&](int k, Tile& t) -> bool {
     const int u = fwd_tile_of_round(k, c, G);
     if (u >= total) return false;
     t.bh = u % p.BH;
+    if constexpr (SPLIT) {
+      t.split = u / p.BH;
+      t.kv_begin = t.split * p.tiles_per_split;
+      t.m0 = 0;
+      t.n0 = min(p.tiles_per_split, n_tiles - t.kv_begin);
+      t.n1 = 0;
+      return true;
+    }
+    t.split = 0;
+    t.kv_begin = 0;
     const int r = u / p.BH;
     const int mblk = CAUSAL ? (p.num_mblocks - 1 - r) : r;
     t.m0 = mblk * 256;
@@ -213,7 +233,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             const CUtensorMap* map = which ? &tmV : &tmK;
             for (int h = 0; h < C::kHalves; ++h)
               ptx::tma_load_3d(sKV(slot) + h * C::kHalfBytes, map, kv_full(slot), h * 64,
-                               j * C::kBlockN, tl.bh);
+                               (tl.kv_begin + j) * C::kBlockN, tl.bh);
           }
         }
       }
@@ -393,10 +413,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         float x[128];
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc) x[cc] = __uint_as_float(raw[cc]);
-        const int kv0 = j * C::kBlockN;
-        const bool edge = (kv0 + C::kBlockN > N) || (CAUSAL && kv0 + C::kBlockN - 1 > m0 + s * C::kBlockM);
+        const int kv0 = (tl.kv_begin + j) * C::kBlockN;
+        // square: query i sees keys 0..i; split: query i of Nq sees keys
+        // 0..Nk-Nq+i (the queries are the last Nq positions)
+        const int diag = SPLIT ? N - p.Nq : m0 + s * C::kBlockM;  // first row's last visible key
+        const bool edge = (kv0 + C::kBlockN > N) || (CAUSAL && kv0 + C::kBlockN - 1 > diag);
         if (edge) {
-          const int lim = (CAUSAL ? min(N, q_idx + 1) : N) - kv0;  // keys [kv0, kv0+lim) visible
+          const int last = SPLIT ? N - p.Nq + q_idx : q_idx;  // this row's last visible key
+          const int lim = (CAUSAL ? min(N, last + 1) : N) - kv0;  // keys [kv0, kv0+lim) visible
 #pragma unroll
           for (int cc = 0; cc < 128; ++cc)
             if (cc >= lim) x[cc] = -INFINITY;
@@ -465,8 +489,34 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // epilogue: O = O_acc / l in bf16, LSE = (m + log2 l) * ln 2.  The next
       // work tile's first P V overwrites O(s) only after this warp's next
       // p_ready arrival, which follows these reads.
-      const bool valid = q_idx < N;
       const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
+      const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
+      const float lse_row = l_run > 0.f ? (m_fin + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
+      if constexpr (SPLIT) {
+        // fp32 partial row of this split, normalised by its own sum.  The
+        // TMEM loads are warp-collective: every lane issues them, only rows
+        // below Nq store.
+        const bool live = q_idx < p.Nq;
+        const size_t prow =
+            (static_cast<size_t>(tl.bh) * p.num_splits + tl.split) * p.Nq + (live ? q_idx : 0);
+        float* orow = p.o_part + prow * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          ptx::tmem_ld_x32(t_o + cc * 32, ov);
+          if (live) {
+            float4* dst = reinterpret_cast<float4*>(orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(ov[4 * v4]) * inv_l, __uint_as_float(ov[4 * v4 + 1]) * inv_l,
+                                    __uint_as_float(ov[4 * v4 + 2]) * inv_l, __uint_as_float(ov[4 * v4 + 3]) * inv_l);
+          }
+        }
+        if (live) p.lse_part[prow] = lse_row;
+        ptx::tc_fence_before();
+        continue;
+      }
+      const bool valid = q_idx < N;
       __nv_bfloat16* orow = p.o + (static_cast<size_t>(tl.bh) * N + (valid ? q_idx : 0)) * D;
 #pragma unroll
       for (int cc = 0; cc < D / 32; ++cc) {
@@ -484,11 +534,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
         }
       }
-      if (valid) {
-        const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
-        p.lse[static_cast<size_t>(tl.bh) * N + q_idx] =
-            l_run > 0.f ? (m_fin + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
-      }
+      if (valid) p.lse[static_cast<size_t>(tl.bh) * N + q_idx] = lse_row;
       ptx::tc_fence_before();
     }
   }

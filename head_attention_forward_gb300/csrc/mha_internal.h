@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <cstddef>
 
 namespace mha_host {
@@ -22,6 +23,14 @@ bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int bo
 // box 64 x min(page_size, 64) x 1 x 1, 128-byte swizzle; out-of-range block
 // ids read as zero.
 bool encode_paged_map(CUtensorMap* map, const void* base, int num_blocks, int H, int page_size, int d);
+
+// The partial pass of split-KV decoding on the tensor cores (the persistent
+// attention kernel in split mode): Nq <= 128 queries per head against Nk
+// keys, num_splits runs of tiles_per_split 128-key tiles, fp32 partial
+// outputs for the merge kernel.  device_setup must have accepted `dev`.
+int fwd_split_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
+                      int BH, int Nq, int Nk, int d, float scale, bool causal, int num_splits,
+                      int tiles_per_split, int dev, unsigned* status, cudaStream_t st);
 
 // Cycle budget of every device-side wait for launches made now.
 long long wait_limit();

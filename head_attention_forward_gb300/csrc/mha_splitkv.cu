@@ -21,6 +21,17 @@ constexpr int kMaxDevices = 64;
 // four waves of two CTAs per SM on a 152-SM part.  A fixed constant keeps the
 // workspace size a pure function of the problem shape.
 constexpr int kTargetCtas = 4 * 2 * 152;
+// The tensor-core partial pass (the persistent attention kernel in split
+// mode, one CTA per SM) takes 128-key tiles; about four (head, split) work
+// tiles per CTA keep its load even.
+constexpr int kTargetTiles = 4 * 152;
+// Contiguous K/V go through the tensor-core pass at d = 128 always, and at
+// d = 64 from three queries on.  The CUDA-core kernel re-reads Q from shared
+// memory for every key, so it falls behind as queries are added; at d = 64
+// with one or two queries it still streams faster (76% vs 55% of HBM
+// bandwidth for one query, measured), because there the tensor-core pass is
+// bound by its softmax rather than by HBM.
+bool use_tensor_path(int Nq, int d) { return d == 128 || Nq >= 3; }
 
 std::mutex g_mu;
 bool g_attr_done[kMaxDevices] = {};
@@ -31,12 +42,15 @@ struct Plan {
 };
 
 // Split count and workspace layout: o_part fp32 [BH, splits, Nq, d], then
-// (16-byte aligned) lse_part fp32 [BH, splits, Nq].
-Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits) {
+// (16-byte aligned) lse_part fp32 [BH, splits, Nq].  Splits are runs of
+// 64-key tiles (CUDA-core pass) or 128-key tiles (tensor-core pass).
+Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits, bool tensor) {
   Plan pl;
-  const int tiles = (Nk + 63) / 64;
+  const int tile_keys = tensor ? 128 : 64;
+  const int target = tensor ? kTargetTiles : kTargetCtas;
+  const int tiles = (Nk + tile_keys - 1) / tile_keys;
   int want = num_splits > 0 ? num_splits
-                            : static_cast<int>(std::max<long long>(1, (kTargetCtas + BH - 1) / BH));
+                            : static_cast<int>(std::max<long long>(1, (target + BH - 1) / BH));
   want = std::max(1, std::min(want, tiles));
   pl.tiles_per_split = (tiles + want - 1) / want;
   pl.splits = (tiles + pl.tiles_per_split - 1) / pl.tiles_per_split;
@@ -87,6 +101,22 @@ cudaError_t launch_partial_d(cudaLaunchConfig_t cfg, const CUtensorMap& mk, cons
   }
 }
 
+// Merge kernel: the splits' partial outputs into O (bf16) and LSE.
+int launch_merge(const float* o_part, const float* lse_part, void* o, float* lse, long long BH,
+                 int Nq, int d, int splits, cudaStream_t st) {
+  cudaLaunchConfig_t mcfg = {};
+  mcfg.gridDim = dim3(static_cast<unsigned>(Nq), static_cast<unsigned>(BH), 1);
+  mcfg.blockDim = dim3(static_cast<unsigned>(d), 1, 1);
+  mcfg.stream = st;
+  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
+  cudaError_t err;
+  if (d == 64)
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, o_part, lse_part, ob, lse, Nq, splits);
+  else
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, o_part, lse_part, ob, lse, Nq, splits);
+  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
 // Partial kernel + merge kernel on `stream` (shared by the contiguous and
 // the paged entry points).
 template <bool PAGED>
@@ -99,18 +129,7 @@ int run_split(const CUtensorMap& mk, const CUtensorMap& mv, mha::SplitParams prm
   cudaError_t err = d == 64 ? launch_partial_d<64, PAGED>(cfg, mk, mv, prm)
                             : launch_partial_d<128, PAGED>(cfg, mk, mv, prm);
   if (err != cudaSuccess) return MHA_ERR_CUDA;
-  cudaLaunchConfig_t mcfg = {};
-  mcfg.gridDim = dim3(static_cast<unsigned>(prm.Nq), static_cast<unsigned>(BH), 1);
-  mcfg.blockDim = dim3(static_cast<unsigned>(d), 1, 1);
-  mcfg.stream = st;
-  __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
-  if (d == 64)
-    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, static_cast<const float*>(prm.o_part),
-                             static_cast<const float*>(prm.lse_part), ob, lse, prm.Nq, pl.splits);
-  else
-    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, static_cast<const float*>(prm.o_part),
-                             static_cast<const float*>(prm.lse_part), ob, lse, prm.Nq, pl.splits);
-  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+  return launch_merge(prm.o_part, prm.lse_part, o, lse, BH, prm.Nq, d, pl.splits, st);
 }
 
 int setup(int* dev, unsigned** status) {
@@ -142,7 +161,10 @@ size_t mha_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_sp
   if (check_shape(B, H, Nq, Nk, d, num_splits) != MHA_OK) return 0;
   const long long BH = static_cast<long long>(B) * H;
   if (BH == 0 || Nq == 0 || Nk == 0) return 0;
-  return make_plan(BH, Nq, Nk, d, num_splits).total;
+  // enough for either partial pass: mha_fwd_paged (always the CUDA-core
+  // pass) takes its workspace size from this function too
+  return std::max(make_plan(BH, Nq, Nk, d, num_splits, true).total,
+                  make_plan(BH, Nq, Nk, d, num_splits, false).total);
 }
 
 int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -158,7 +180,8 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(workspace))
     return MHA_ERR_MISALIGNED;
-  const Plan pl = make_plan(BH, Nq, Nk, d, num_splits);
+  const bool tensor = use_tensor_path(Nq, d);
+  const Plan pl = make_plan(BH, Nq, Nk, d, num_splits, tensor);
   if (workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
   const size_t qb = static_cast<size_t>(BH) * Nq * d * 2, kb = static_cast<size_t>(BH) * Nk * d * 2;
   const size_t lb = static_cast<size_t>(BH) * Nq * 4;
@@ -177,6 +200,16 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
   unsigned* status = nullptr;
   rc = setup(&dev, &status);
   if (rc != MHA_OK) return rc;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                             ((pl.o_part_bytes + 15) & ~static_cast<size_t>(15)));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (tensor) {
+    rc = fwd_split_partial(q, k, v, o_part, lse_part, static_cast<int>(BH), Nq, Nk, d, scale,
+                           causal != 0, pl.splits, pl.tiles_per_split, dev, status, st);
+    if (rc != MHA_OK) return rc;
+    return launch_merge(o_part, lse_part, o, lse, BH, Nq, d, pl.splits, st);
+  }
   CUtensorMap mk, mv;
   if (!encode_map(&mk, k, static_cast<int>(BH), Nk, d, 64) ||
       !encode_map(&mv, v, static_cast<int>(BH), Nk, d, 64))
@@ -218,7 +251,7 @@ int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const
       !aligned16(lse) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3))
     return MHA_ERR_MISALIGNED;
-  const Plan pl = make_plan(BH, Nq, static_cast<int>(max_keys), d, num_splits);
+  const Plan pl = make_plan(BH, Nq, static_cast<int>(max_keys), d, num_splits, false);
   if (workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
   const size_t qb = static_cast<size_t>(BH) * Nq * d * 2;
   const size_t cb = static_cast<size_t>(num_blocks) * H * page_size * d * 2;

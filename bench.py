@@ -391,7 +391,9 @@ def run_paged(args, name):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": src, "traffic": recorded_traffic(name),
                      "algorithmic_bytes_per_step": algo_bytes,
-                     "kernel": f"splitkv_partial_kernel<{d},paged> + splitkv_merge_kernel<{d}>"},
+                     "kernel": (f"mha_fwd_kernel<{d},{int(bool(causal))},split,paged> + splitkv_merge_kernel<{d}>"
+                                if (d == 128 or Nq >= 3) else  # the library's choice of partial pass
+                                f"splitkv_partial_kernel<{d},paged> + splitkv_merge_kernel<{d}>")},
         "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
     }), flush=True)
     return 0

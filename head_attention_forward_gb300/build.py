@@ -16,7 +16,7 @@ LIB = os.path.join(PKG, "_build", "libmha_fwd.so")
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
     "-I", os.path.join(ROOT, "include"),
 ]
 
@@ -36,10 +36,26 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = os.environ.get("NVCC", "nvcc")
     if not os.path.isabs(nvcc) and os.path.exists("/usr/local/cuda/bin/nvcc"):
         nvcc = "/usr/local/cuda/bin/nvcc"
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [nvcc] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-o", tmp] + SOURCES
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    tag = f".tmp{os.getpid()}"
+    # one nvcc per translation unit, all at once, then one link
+    objs, procs = [], []
+    for src in SOURCES:
+        obj = os.path.join(os.path.dirname(LIB), os.path.basename(src)[:-3] + tag + ".o")
+        cmd = [nvcc] + NVCC_FLAGS + (["-Xptxas", "-v"] if verbose else []) + ["-c", src, "-o", obj]
+        objs.append(obj)
+        procs.append((subprocess.Popen(cmd), cmd))
+    failed = [cmd for proc, cmd in procs if proc.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        tmp = LIB + tag
+        subprocess.run([nvcc, "-gencode", "arch=compute_103a,code=sm_103a", "-shared", "-o", tmp] + objs,
+                       check=True)
+        os.replace(tmp, LIB)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     return LIB
 
 

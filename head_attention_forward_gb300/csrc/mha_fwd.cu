@@ -84,6 +84,10 @@ int device_setup(int* dev_out, unsigned** status_out) {
     smem_attr(mha::mha_fwd_kernel<64, true, true>, mha::FwdCfg<64>::kSmemBytes);
     smem_attr(mha::mha_fwd_kernel<128, false, true>, mha::FwdCfg<128>::kSmemBytes);
     smem_attr(mha::mha_fwd_kernel<128, true, true>, mha::FwdCfg<128>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, false, true, true>, mha::FwdCfg<64>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, true, true, true>, mha::FwdCfg<64>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, false, true, true>, mha::FwdCfg<128>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, true, true, true>, mha::FwdCfg<128>::kSmemBytes);
     void* sym = nullptr;
     fail |= cudaGetSymbolAddress(&sym, g_status) != cudaSuccess;
     fail |= cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -121,13 +125,13 @@ bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int bo
 }
 
 bool encode_paged_map(CUtensorMap* map, const void* base, int num_blocks, int H, int page_size,
-                      int d) {
+                      int d, int box_rows) {
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(page_size),
                         static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(num_blocks)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(page_size) * d * 2,
                            static_cast<cuuint64_t>(H) * page_size * d * 2};
-  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(page_size < 64 ? page_size : 64), 1, 1};
+  cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   cuuint32_t estride[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -151,16 +155,26 @@ long long wait_limit() {
 }  // namespace mha_host
 
 namespace {
-template <int D, bool CAUSAL, bool SPLIT>
+template <int D, bool CAUSAL, bool SPLIT, bool PAGED>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                    const mha::FwdParams& prm, int sms, cudaStream_t stream);
+
+template <bool PAGED>
+cudaError_t launch_split(int d, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
+                         const CUtensorMap& mv, const mha::FwdParams& prm, int sms, cudaStream_t st) {
+  if (d == 64)
+    return causal ? launch<64, true, true, PAGED>(mq, mk, mv, prm, sms, st)
+                  : launch<64, false, true, PAGED>(mq, mk, mv, prm, sms, st);
+  return causal ? launch<128, true, true, PAGED>(mq, mk, mv, prm, sms, st)
+                : launch<128, false, true, PAGED>(mq, mk, mv, prm, sms, st);
+}
 }  // namespace
 
 namespace mha_host {
 
 int fwd_split_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
-                      int BH, int Nq, int Nk, int d, float scale, bool causal, int num_splits,
-                      int tiles_per_split, int dev, unsigned* status, cudaStream_t st) {
+                      int* tile_counter, int BH, int Nq, int Nk, int d, float scale, bool causal,
+                      int num_splits, int tiles_per_split, int dev, unsigned* status, cudaStream_t st) {
   CUtensorMap mq, mk, mv;
   if (!encode_map(&mq, q, BH, Nq, d, 128) || !encode_map(&mk, k, BH, Nk, d, 128) ||
       !encode_map(&mv, v, BH, Nk, d, 128))
@@ -177,15 +191,47 @@ int fwd_split_partial(const void* q, const void* k, const void* v, float* o_part
   prm.tiles_per_split = tiles_per_split;
   prm.o_part = o_part;
   prm.lse_part = lse_part;
+  prm.tile_counter = tile_counter;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  const int sms = device_sms(dev);
-  cudaError_t err;
-  if (d == 64)
-    err = causal ? launch<64, true, true>(mq, mk, mv, prm, sms, st)
-                 : launch<64, false, true>(mq, mk, mv, prm, sms, st);
-  else
-    err = causal ? launch<128, true, true>(mq, mk, mv, prm, sms, st)
-                 : launch<128, false, true>(mq, mk, mv, prm, sms, st);
+  if (cudaMemsetAsync(tile_counter, 0, sizeof(int), st) != cudaSuccess) return MHA_ERR_CUDA;
+  const cudaError_t err = launch_split<false>(d, causal, mq, mk, mv, prm, device_sms(dev), st);
+  return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
+}
+
+int fwd_paged_partial(const void* q, const void* k_cache, const void* v_cache,
+                      const int* block_table, const int* seq_lens, float* o_part, float* lse_part,
+                      int* tile_counter, int B, int H, int Nq, int d, int page_size, int num_blocks,
+                      int max_blocks, float scale, bool causal, int num_splits, int tiles_per_split, int dev,
+                      unsigned* status, cudaStream_t st) {
+  const int BH = B * H;
+  const int rows = page_size < 128 ? page_size : 128;
+  CUtensorMap mq, mk, mv;
+  if (!encode_map(&mq, q, BH, Nq, d, 128) ||
+      !encode_paged_map(&mk, k_cache, num_blocks, H, page_size, d, rows) ||
+      !encode_paged_map(&mv, v_cache, num_blocks, H, page_size, d, rows))
+    return MHA_ERR_CUDA;
+  mha::FwdParams prm = {};
+  prm.status = status;
+  prm.wait_limit = wait_limit();
+  prm.N = max_blocks * page_size;
+  prm.num_mblocks = 1;
+  prm.BH = BH;
+  prm.Nq = Nq;
+  prm.Nk = max_blocks * page_size;
+  prm.num_splits = num_splits;
+  prm.tiles_per_split = tiles_per_split;
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
+  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  prm.block_table = block_table;
+  prm.seq_lens = seq_lens;
+  prm.page_size = page_size;
+  prm.max_blocks = max_blocks;
+  prm.num_heads = H;
+  prm.num_blocks = num_blocks;
+  prm.tile_counter = tile_counter;
+  if (cudaMemsetAsync(tile_counter, 0, sizeof(int), st) != cudaSuccess) return MHA_ERR_CUDA;
+  const cudaError_t err = launch_split<true>(d, causal, mq, mk, mv, prm, device_sms(dev), st);
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
@@ -196,7 +242,7 @@ using namespace mha_host;
 
 // Persistent launch: one CTA per SM (fewer when there are fewer work tiles),
 // each walking its share of the (bh, m-block) or (bh, split) tiles.
-template <int D, bool CAUSAL, bool SPLIT = false>
+template <int D, bool CAUSAL, bool SPLIT = false, bool PAGED = false>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                    const mha::FwdParams& prm, int sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -207,7 +253,7 @@ cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, mha::mha_fwd_kernel<D, CAUSAL, SPLIT>, mq, mk, mv, prm);
+  return cudaLaunchKernelEx(&cfg, mha::mha_fwd_kernel<D, CAUSAL, SPLIT, PAGED>, mq, mk, mv, prm);
 }
 
 }  // namespace

@@ -70,6 +70,14 @@ struct FwdParams {
   float* o_part;       // [BH, num_splits, Nq, D]
   float* lse_part;     // [BH, num_splits, Nq]
   float scale_log2;    // scale * log2(e)
+  // paged mode only (split mode over a paged cache): key t of batch entry
+  // b = bh / num_heads is row t % page_size of cache block
+  // block_table[b * max_blocks + t / page_size]; the entry holds
+  // min(seq_lens[b], max_blocks * page_size) keys and Nk is that bound
+  const int* block_table;  // [B, max_blocks]
+  const int* seq_lens;     // [B]
+  int page_size, max_blocks, num_heads, num_blocks;
+  int* tile_counter;       // split mode: work tiles handed out so far past the grid (zero at launch)
 };
 
 template <int D>
@@ -86,9 +94,16 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQSets * 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  // split mode: ring of work-tile ids from the K/V producer to the other
+  // roles (Q producer, MMA issuer, eight softmax warps)
+  static constexpr int kTileRing = 8;
+  static constexpr int kTileConsumers = 1 + 1 + 8;
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_ready[2] o_full[2] drain
-  static constexpr int kNumBars = 4 + 2 * kStages + 2 + 2 + 2 + 1;
-  static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
+  // tail (paged mode: the copy of a V tile whose last rows get cleared)
+  // tile_full[R] tile_empty[R]
+  static constexpr int kNumBars = 4 + 2 * kStages + 2 + 2 + 2 + 1 + 1 + 2 * kTileRing;
+  static constexpr int kOffTileIds = kOffBar + 8 * kNumBars;
+  static constexpr int kOffTmemSlot = kOffTileIds + 4 * kTileRing;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
@@ -111,12 +126,18 @@ __device__ __forceinline__ int fwd_tile_of_round(int k, int c, int G) {
 
 // SPLIT = false: the attention forward pass (square, top-left causal mask).
 // SPLIT = true: the partial pass of split-KV decoding (bottom-right causal
-// mask, fp32 partial outputs for splitkv_merge_kernel); only stage 0 is used.
-template <int D, bool CAUSAL, bool SPLIT = false>
+// mask, fp32 partial outputs for splitkv_merge_kernel); only stage 0 is used,
+// the Q buffers of both stages serve as two Q sets, and work tiles are
+// handed out at run time.
+// PAGED = true (with SPLIT): the same pass over a paged K/V cache, each
+// batch entry with its own key count; tmK / tmV are then 4-D maps
+// [blocks][heads][page rows][d] with boxes of min(page_size, 128) rows.
+template <int D, bool CAUSAL, bool SPLIT = false, bool PAGED = false>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     mha_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
   using C = FwdCfg<D>;
+  static_assert(SPLIT || !PAGED, "the paged pass is a split pass");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -133,22 +154,33 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   auto tiles_for = [&](int row0) {
     return row0 >= N ? 0 : (CAUSAL ? min(n_tiles, row0 / C::kBlockN + 1) : n_tiles);
   };
-  // the k-th tile of this CTA: head, first query row, K/V tiles per stage
+  // a work tile: head, first query row, K/V tiles per stage, keys of the
+  // head (split mode: n0 is 0 for a split past them)
   struct Tile {
-    int bh, m0, n0, n1, kv_begin, split;
+    int bh, m0, n0, n1, kv_begin, split, nk;
   };
+  // split mode: tile u is split u / BH of head bh = u % BH, so the heads of
+  // one batch entry (bh = b * heads + h) are adjacent.  Every tile runs on
+  // stage 0 (running odd tiles on stage 1, so that one tile's epilogue
+  // overlaps the next one's start, measured 2-3% slower).
+  auto keys_of = [&](int bh) {
+    return PAGED ? max(0, min(p.seq_lens[bh / p.num_heads], p.max_blocks * p.page_size)) : N;
+  };
+  auto split_tile = [&](int u, Tile& t) {
+    t.bh = u % p.BH;
+    t.split = u / p.BH;
+    t.kv_begin = t.split * p.tiles_per_split;
+    t.m0 = 0;
+    t.nk = keys_of(t.bh);
+    t.n0 = max(0, min(p.tiles_per_split, (t.nk + C::kBlockN - 1) / C::kBlockN - t.kv_begin));
+    t.n1 = 0;
+  };
+  // square mode: the k-th tile of this CTA in the static order
   auto tile_at = [&](int k, Tile& t) -> bool {
     const int u = fwd_tile_of_round(k, c, G);
     if (u >= total) return false;
     t.bh = u % p.BH;
-    if constexpr (SPLIT) {
-      t.split = u / p.BH;
-      t.kv_begin = t.split * p.tiles_per_split;
-      t.m0 = 0;
-      t.n0 = min(p.tiles_per_split, n_tiles - t.kv_begin);
-      t.n1 = 0;
-      return true;
-    }
+    t.nk = N;
     t.split = 0;
     t.kv_begin = 0;
     const int r = u / p.BH;
@@ -160,24 +192,56 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   };
 
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
-  // Q set b holds work tiles b, b + kQSets, ...: the m-th use of a set is
-  // phase m of its barriers
-  auto q_full = [&](int b) { return bar(b); };       // both stages' Q tiles loaded
+  // Q set b holds work tiles b, b + kQS, ...: the m-th use of a set is
+  // phase m of its barriers.  Split mode needs one Q tile per work tile,
+  // so the buffers of both stages make two sets.
+  constexpr int kQS = SPLIT ? 2 : C::kQSets;
+  auto q_full = [&](int b) { return bar(b); };       // the work tile's Q tiles loaded
   auto q_empty = [&](int b) { return bar(2 + b); };  // every S MMA reading them done
-  auto q_set = [](int k) { return k % C::kQSets; };
-  auto q_par = [](int k) { return (k / C::kQSets) & 1; };
+  auto q_set = [](int k) { return k % kQS; };
+  auto q_par = [](int k) { return (k / kQS) & 1; };
   auto kv_full = [&](int i) { return bar(4 + i); };
   auto kv_empty = [&](int i) { return bar(4 + C::kStages + i); };
   auto s_full = [&](int s) { return bar(4 + 2 * C::kStages + s); };
   auto p_ready = [&](int s) { return bar(6 + 2 * C::kStages + s); };
   auto o_full = [&](int s) { return bar(8 + 2 * C::kStages + s); };
   const uint32_t drain_bar = bar(10 + 2 * C::kStages);
-  auto sQ = [&](int b, int s) -> uint32_t { return sbase + C::kOffQ + (2 * b + s) * C::kTileBytes; };
+  const uint32_t tail_bar = bar(11 + 2 * C::kStages);
+  auto tile_full = [&](int i) { return bar(12 + 2 * C::kStages + i); };
+  auto tile_empty = [&](int i) { return bar(12 + 2 * C::kStages + C::kTileRing + i); };
+  int* tile_ids = reinterpret_cast<int*>(smem + C::kOffTileIds);
+  // Q tile of set b, stage s
+  auto q_index = [](int b, int s) { return SPLIT ? b : 2 * b + s; };
+  auto sQ = [&](int b, int s) -> uint32_t { return sbase + C::kOffQ + q_index(b, s) * C::kTileBytes; };
   auto sKV = [&](int i) -> uint32_t { return sbase + C::kOffKV + i * C::kTileBytes; };
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit};
+
+  // The k-th work tile of this CTA, for every role but the K/V producer.
+  // Square mode: the static order.  Split mode: the k-th id the K/V
+  // producer put in the ring (an id >= total ends the work).  One thread
+  // (warp_wide false) or a whole warp calls it; false at the end of the
+  // work, or with ok = false when a wait gave up.
+  auto take_tile = [&](int k, Tile& t, bool& ok, bool warp_wide, unsigned site) -> bool {
+    if constexpr (!SPLIT) {
+      return tile_at(k, t);
+    } else {
+      const int slot = k % C::kTileRing;
+      const uint32_t par = (k / C::kTileRing) & 1;
+      if (!(warp_wide ? wait_warp(tile_full(slot), par, ctl, site) : wait_one(tile_full(slot), par, ctl, site))) {
+        ok = false;
+        return false;
+      }
+      const int u = tile_ids[slot];
+      if (warp_wide) __syncwarp();
+      if (!warp_wide || lane == 0) ptx::mbar_arrive(tile_empty(slot));
+      if (u >= total) return false;
+      split_tile(u, t);
+      return true;
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -194,6 +258,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       ptx::mbar_init(o_full(s), 1);
     }
     ptx::mbar_init(drain_bar, 1);
+    ptx::mbar_init(tail_bar, 1);
+    for (int i = 0; i < C::kTileRing; ++i) {
+      ptx::mbar_init(tile_full(i), 1);
+      ptx::mbar_init(tile_empty(i), C::kTileConsumers);  // one arrive per consumer warp
+    }
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -214,34 +283,160 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   if (warp == 0) {
     // -------------------------------------------------- K/V producer
     // K_j, V_j of every work tile in turn through one ring; position t
-    // runs on across work tiles.
-    if (lane == 0) {
-      int t = 0;
-      bool ok = true;
-      Tile tl;
-      for (int k = 0; ok && tile_at(k, tl); ++k) {
-        const int n_kv = max(tl.n0, tl.n1);
-        for (int j = 0; j < n_kv && ok; ++j) {
-          for (int which = 0; which < 2; ++which, ++t) {
-            const int slot = t % C::kStages;
-            const int use = t / C::kStages;
-            if (use > 0 && !wait_one(kv_empty(slot), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
-              ok = false;
-              break;
-            }
-            ptx::mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
-            const CUtensorMap* map = which ? &tmV : &tmK;
-            for (int h = 0; h < C::kHalves; ++h)
-              ptx::tma_load_3d(sKV(slot) + h * C::kHalfBytes, map, kv_full(slot), h * 64,
-                               (tl.kv_begin + j) * C::kBlockN, tl.bh);
+    // runs on across work tiles.  The whole warp walks the loop (its waits
+    // stay warp-uniform) and one lane issues the copies.
+    int t = 0;
+    int scrubs = 0;  // tail_bar phases used
+    bool ok = true;
+    // paged mode: a K or V tile is `chunks` boxes of `rows` keys, each from
+    // the page its first key lies in; lane r < chunks issues box r.  Each
+    // lane reads its block id one K/V tile ahead (and the first one of the
+    // next work tile while this one's last copies land), so the table's
+    // latency overlaps the ring waits instead of adding to them.
+    const int rows = PAGED ? min(p.page_size, C::kBlockN) : C::kBlockN;
+    const int chunks = C::kBlockN / rows;
+    auto block_of = [&](const Tile& w, int j) -> int {
+      const int pos = (w.kv_begin + j) * C::kBlockN + lane * rows;
+      // a page past the entry's length reads as zeros (a block id past the
+      // cache); pos < nk also keeps the table read inside its row
+      if (lane >= chunks || pos >= w.nk) return p.num_blocks;
+      return p.block_table[static_cast<size_t>(w.bh / p.num_heads) * p.max_blocks + pos / p.page_size];
+    };
+    // split mode: this warp draws the work tiles (the first one is the
+    // CTA's index, each further one comes from the global counter once the
+    // current tile's last copy is issued) and hands their ids to the other
+    // roles through the ring
+    int published = 0;
+    auto publish = [&](int u) -> bool {
+      const int slot = published % C::kTileRing;
+      if (published >= C::kTileRing &&
+          !wait_warp(tile_empty(slot), ((published / C::kTileRing) - 1) & 1, ctl, kSiteProducerEmpty))
+        return false;
+      if (lane == 0) {
+        tile_ids[slot] = u;
+        ptx::mbar_arrive(tile_full(slot));  // release: the id is visible to whoever sees the phase
+      }
+      __syncwarp();
+      ++published;
+      return true;
+    };
+    auto empty_split = [&](int u) {
+      return (u / p.BH) * p.tiles_per_split * C::kBlockN >= keys_of(u % p.BH);
+    };
+    auto draw = [&]() -> int {
+      int u = 0;
+      if (lane == 0) {
+        u = G + atomicAdd(p.tile_counter, 1);
+        if constexpr (PAGED) {
+          // a split past an entry's keys is past them for every head of the
+          // entry: move the counter beyond that run of heads
+          while (u < total && empty_split(u)) {
+            atomicMax(p.tile_counter, u - u % p.num_heads + p.num_heads - G);
+            u = G + atomicAdd(p.tile_counter, 1);
           }
         }
       }
-      if (!ok) {
-        // let the copies already issued land before the CTA goes away
-        for (int u = max(0, t - C::kStages); u < t; ++u)
-          drain_wait(kv_full(u % C::kStages), (u / C::kStages) & 1, ctl);
+      return __shfl_sync(0xffffffffu, u, 0);
+    };
+    Tile tl;
+    bool have;
+    if constexpr (SPLIT) {
+      int u = c;
+      if (PAGED && empty_split(u)) u = draw();
+      ok = publish(u);
+      have = ok && u < total;
+      if (have) split_tile(u, tl);
+    } else {
+      have = tile_at(0, tl);
+    }
+    int blk_next = (PAGED && have) ? block_of(tl, 0) : 0;
+    for (int k = 0; ok && have; ++k) {
+      const int n_kv = max(tl.n0, tl.n1);
+      // split mode: the next tile is drawn once this one's last copy is
+      // issued (drawing it two K/V tiles earlier measured the same)
+      int u_next = total;
+      if (SPLIT && n_kv == 0) {
+        u_next = draw();
+        ok = publish(u_next);
       }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int key0 = (tl.kv_begin + j) * C::kBlockN;
+        const int blk = blk_next;
+        if (PAGED && j + 1 < n_kv) blk_next = block_of(tl, j + 1);
+        for (int which = 0; which < 2; ++which, ++t) {
+          const int slot = t % C::kStages;
+          const int use = t / C::kStages;
+          if (use > 0 && !wait_warp(kv_empty(slot), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
+            ok = false;
+            break;
+          }
+          const CUtensorMap* map = which ? &tmV : &tmK;
+          if constexpr (PAGED) {
+            // every box lands 1 KiB aligned, so the 128-byte swizzle of the
+            // tile is that of one 128-row box
+            const int valid = tl.nk - key0;  // keys of this tile inside the entry (>= 1)
+            // V rows past the entry's length that come from its last,
+            // partly filled page hold whatever the cache holds there,
+            // possibly NaN, and a zero weight times NaN is NaN: that copy
+            // lands on tail_bar, the rows get cleared, and only then is the
+            // slot marked full (masked scores make the same rows of K harmless)
+            const bool scrub = which == 1 && valid < C::kBlockN && valid % rows != 0;
+            const uint32_t done = scrub ? tail_bar : kv_full(slot);
+            if (lane == 0) ptx::mbar_arrive_expect_tx(done, C::kTileBytes);
+            __syncwarp();
+            if (lane < chunks) {
+              const int head = tl.bh % p.num_heads;
+              const int pos = key0 + lane * rows;
+              for (int h = 0; h < C::kHalves; ++h)
+                ptx::tma_load_4d(sKV(slot) + h * C::kHalfBytes + lane * rows * 128, map, done, h * 64,
+                                 pos % p.page_size, head, blk);
+            }
+            __syncwarp();
+            if (scrub) {
+              if (!wait_warp(tail_bar, scrubs & 1, ctl, kSiteProducerEmpty)) {
+                if (lane == 0) drain_wait(tail_bar, scrubs & 1, ctl);
+                ok = false;
+                break;
+              }
+              ++scrubs;
+              uint8_t* vt = smem + C::kOffKV + slot * C::kTileBytes;
+              const int n16 = (C::kBlockN - valid) * 8;  // 16-byte pieces per half
+              for (int i = lane; i < C::kHalves * n16; i += 32) {
+                const int h = i / n16, r = i - h * n16;
+                *reinterpret_cast<uint4*>(vt + h * C::kHalfBytes + valid * 128 + r * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+              }
+              ptx::fence_proxy_async_smem();  // visible to the tensor core's reads
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(kv_full(slot));
+            }
+          } else {
+            if (lane == 0) {
+              ptx::mbar_arrive_expect_tx(kv_full(slot), C::kTileBytes);
+              for (int h = 0; h < C::kHalves; ++h)
+                ptx::tma_load_3d(sKV(slot) + h * C::kHalfBytes, map, kv_full(slot), h * 64, key0, tl.bh);
+            }
+            __syncwarp();
+          }
+        }
+        if (SPLIT && ok && j == n_kv - 1) {
+          u_next = draw();
+          ok = publish(u_next);
+        }
+      }
+      if (!ok) break;
+      if constexpr (SPLIT) {
+        have = u_next < total;
+        if (have) split_tile(u_next, tl);
+      } else {
+        have = tile_at(k + 1, tl);
+      }
+      if (PAGED && have) blk_next = block_of(tl, 0);
+    }
+    if (!ok && lane == 0) {
+      // let the copies already issued land before the CTA goes away
+      for (int u = max(0, t - C::kStages); u < t; ++u)
+        drain_wait(kv_full(u % C::kStages), (u / C::kStages) & 1, ctl);
     }
     __syncwarp();
   } else if (warp == 2) {
@@ -251,25 +446,27 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     // epilogue.
     if (lane == 0) {
       Tile tl;
-      int k = 0;
+      int kq = 0;  // work tiles with K/V tiles so far: the sets go to those only
       bool ok = true;
-      for (; ok && tile_at(k, tl); ++k) {
-        // the set's previous tile (k - kQSets) must be done with it
-        const int prev = k - C::kQSets;
+      for (int k = 0; ok && take_tile(k, tl, ok, false, kSiteProducerEmpty); ++k) {
+        if (max(tl.n0, tl.n1) == 0) continue;  // a split past the head's keys
+        // the set's previous tile (kq - kQSets) must be done with it
+        const int prev = kq - kQS;
         if (prev >= 0 && !wait_one(q_empty(q_set(prev)), q_par(prev), ctl, kSiteProducerEmpty)) {
           ok = false;
           break;
         }
-        const int b = q_set(k);
-        const int stages = tl.n1 > 0 ? 2 : 1;
+        const int b = q_set(kq);
+        const int stages = (!SPLIT && tl.n1 > 0) ? 2 : 1;  // split mode: one Q tile
         ptx::mbar_arrive_expect_tx(q_full(b), stages * C::kTileBytes);
         for (int s = 0; s < stages; ++s)
           for (int h = 0; h < C::kHalves; ++h)
             ptx::tma_load_3d(sQ(b, s) + h * C::kHalfBytes, &tmQ, q_full(b), h * 64,
                              tl.m0 + s * C::kBlockM, tl.bh);
+        ++kq;
       }
       if (!ok)
-        for (int u = max(0, k - C::kQSets); u < k; ++u) drain_wait(q_full(q_set(u)), q_par(u), ctl);
+        for (int u = max(0, kq - kQS); u < kq; ++u) drain_wait(q_full(q_set(u)), q_par(u), ctl);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -298,7 +495,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // S(s) = Q_s K^T over K = d in steps of 16
       auto issue_s = [&](int qb, int s, int kslot) {
         const uint64_t dk = dK0 + slot_off(kslot);
-        const uint64_t dq = dQ00 + static_cast<uint64_t>(((2 * qb + s) * C::kTileBytes) >> 4);
+        const uint64_t dq = dQ00 + static_cast<uint64_t>((q_index(qb, s) * C::kTileBytes) >> 4);
         const uint32_t ts = s ? tS1 : tS0;
         if (ptx::elect_one()) {
 #pragma unroll
@@ -331,11 +528,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       int t = 0;                 // K/V ring position
       int pr[2] = {0, 0};        // p_ready completions consumed, per stage
       Tile tl;
-      for (int k = 0; ok && tile_at(k, tl); ++k) {
+      int kq = 0;                // work tiles with K/V tiles so far (Q set uses)
+      for (int k = 0; ok && take_tile(k, tl, ok, true, kSiteMmaQ); ++k) {
         auto n_s = [&](int s) { return s ? tl.n1 : tl.n0; };
         const int n_kv = max(tl.n0, tl.n1);
-        const int qb = q_set(k);
-        if (!(ok = wait_warp(q_full(qb), q_par(k), ctl, kSiteMmaQ))) break;
+        if (n_kv == 0) continue;  // a split past the head's keys
+        const int qb = q_set(kq);
+        if (!(ok = wait_warp(q_full(qb), q_par(kq), ctl, kSiteMmaQ))) break;
+        ++kq;
         int v_prev = 0;
         for (int j = 0; j < n_kv && ok; ++j) {
           const int k_slot = t % C::kStages, k_par = (t / C::kStages) & 1;
@@ -394,7 +594,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     int sf = 0;  // s_full completions consumed
     int of = 0;  // o_full completions consumed
     Tile tl;
-    for (int k = 0; ok && tile_at(k, tl); ++k) {
+    for (int k = 0; ok && take_tile(k, tl, ok, true, kSiteSoftmaxS); ++k) {
       const int m0 = tl.m0;
       const int n = s ? tl.n1 : tl.n0;
       const int q_idx = m0 + s * C::kBlockM + row;
@@ -414,13 +614,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc) x[cc] = __uint_as_float(raw[cc]);
         const int kv0 = (tl.kv_begin + j) * C::kBlockN;
+        const int nk = tl.nk;  // keys of this head
         // square: query i sees keys 0..i; split: query i of Nq sees keys
-        // 0..Nk-Nq+i (the queries are the last Nq positions)
-        const int diag = SPLIT ? N - p.Nq : m0 + s * C::kBlockM;  // first row's last visible key
-        const bool edge = (kv0 + C::kBlockN > N) || (CAUSAL && kv0 + C::kBlockN - 1 > diag);
+        // 0..nk-Nq+i (the queries are the last Nq positions)
+        const int diag = SPLIT ? nk - p.Nq : m0 + s * C::kBlockM;  // first row's last visible key
+        const bool edge = (kv0 + C::kBlockN > nk) || (CAUSAL && kv0 + C::kBlockN - 1 > diag);
         if (edge) {
-          const int last = SPLIT ? N - p.Nq + q_idx : q_idx;  // this row's last visible key
-          const int lim = (CAUSAL ? min(N, last + 1) : N) - kv0;  // keys [kv0, kv0+lim) visible
+          const int last = SPLIT ? nk - p.Nq + q_idx : q_idx;  // this row's last visible key
+          const int lim = (CAUSAL ? min(nk, last + 1) : nk) - kv0;  // keys [kv0, kv0+lim) visible
 #pragma unroll
           for (int cc = 0; cc < 128; ++cc)
             if (cc >= lim) x[cc] = -INFINITY;

@@ -22,11 +22,14 @@ constexpr int kMaxDevices = 64;
 // workspace size a pure function of the problem shape.
 constexpr int kTargetCtas = 4 * 2 * 152;
 // The tensor-core partial pass (the persistent attention kernel in split
-// mode, one CTA per SM) takes 128-key tiles; about four (head, split) work
-// tiles per CTA keep its load even.
-constexpr int kTargetTiles = 4 * 152;
-// Contiguous K/V go through the tensor-core pass at d = 128 always, and at
-// d = 64 from three queries on.  The CUDA-core kernel re-reads Q from shared
+// mode, one CTA per SM) takes 128-key tiles and hands (head, split) work
+// tiles out at run time.  Each work tile costs a pipeline drain at its end,
+// so fewer, longer ones do better until the last ones leave CTAs idle:
+// about six per CTA measured best on decode shapes (88-98% of the HBM copy
+// rate against 84-88% with 32 per CTA).
+constexpr int kTargetTiles = 6 * 152;
+// K/V (contiguous or paged) go through the tensor-core pass at d = 128
+// always, and at d = 64 from three queries on.  The CUDA-core kernel re-reads Q from shared
 // memory for every key, so it falls behind as queries are added; at d = 64
 // with one or two queries it still streams faster (76% vs 55% of HBM
 // bandwidth for one query, measured), because there the tensor-core pass is
@@ -37,13 +40,15 @@ std::mutex g_mu;
 bool g_attr_done[kMaxDevices] = {};
 
 struct Plan {
-  int splits = 0, tiles_per_split = 0;
-  size_t o_part_bytes = 0, lse_part_bytes = 0, total = 0;
+  int splits = 0, tiles_per_split = 0, tile_keys = 0;
+  size_t o_part_bytes = 0, lse_part_bytes = 0, lse_off = 0, counter_off = 0, total = 0;
 };
 
 // Split count and workspace layout: o_part fp32 [BH, splits, Nq, d], then
-// (16-byte aligned) lse_part fp32 [BH, splits, Nq].  Splits are runs of
-// 64-key tiles (CUDA-core pass) or 128-key tiles (tensor-core pass).
+// (16-byte aligned) lse_part fp32 [BH, splits, Nq], then (16-byte aligned)
+// the tensor-core pass's work-tile counter (one int in 16 bytes).  Splits
+// are runs of 64-key tiles (CUDA-core pass) or 128-key tiles (tensor-core
+// pass).
 Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits, bool tensor) {
   Plan pl;
   const int tile_keys = tensor ? 128 : 64;
@@ -54,9 +59,12 @@ Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits, bool tensor)
   want = std::max(1, std::min(want, tiles));
   pl.tiles_per_split = (tiles + want - 1) / want;
   pl.splits = (tiles + pl.tiles_per_split - 1) / pl.tiles_per_split;
+  pl.tile_keys = tile_keys;
   pl.o_part_bytes = static_cast<size_t>(BH) * pl.splits * Nq * d * 4;
   pl.lse_part_bytes = static_cast<size_t>(BH) * pl.splits * Nq * 4;
-  pl.total = ((pl.o_part_bytes + 15) & ~static_cast<size_t>(15)) + pl.lse_part_bytes;
+  pl.lse_off = (pl.o_part_bytes + 15) & ~static_cast<size_t>(15);
+  pl.counter_off = (pl.lse_off + pl.lse_part_bytes + 15) & ~static_cast<size_t>(15);
+  pl.total = pl.counter_off + 16;
   return pl;
 }
 
@@ -101,9 +109,16 @@ cudaError_t launch_partial_d(cudaLaunchConfig_t cfg, const CUtensorMap& mk, cons
   }
 }
 
+// Paged caches: what the merge needs to count each entry's splits.
+struct PagedSplits {
+  const int* seq_lens = nullptr;  // null: every head has all the splits
+  int num_heads = 1, max_keys = 0;
+  long long split_keys = 1;       // keys per split
+};
+
 // Merge kernel: the splits' partial outputs into O (bf16) and LSE.
 int launch_merge(const float* o_part, const float* lse_part, void* o, float* lse, long long BH,
-                 int Nq, int d, int splits, cudaStream_t st) {
+                 int Nq, int d, int splits, cudaStream_t st, const PagedSplits& ps = PagedSplits()) {
   cudaLaunchConfig_t mcfg = {};
   mcfg.gridDim = dim3(static_cast<unsigned>(Nq), static_cast<unsigned>(BH), 1);
   mcfg.blockDim = dim3(static_cast<unsigned>(d), 1, 1);
@@ -111,9 +126,11 @@ int launch_merge(const float* o_part, const float* lse_part, void* o, float* lse
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
   cudaError_t err;
   if (d == 64)
-    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, o_part, lse_part, ob, lse, Nq, splits);
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, o_part, lse_part, ob, lse, Nq, splits,
+                             ps.seq_lens, ps.num_heads, ps.split_keys, ps.max_keys);
   else
-    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, o_part, lse_part, ob, lse, Nq, splits);
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, o_part, lse_part, ob, lse, Nq, splits,
+                             ps.seq_lens, ps.num_heads, ps.split_keys, ps.max_keys);
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
@@ -161,8 +178,8 @@ size_t mha_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_sp
   if (check_shape(B, H, Nq, Nk, d, num_splits) != MHA_OK) return 0;
   const long long BH = static_cast<long long>(B) * H;
   if (BH == 0 || Nq == 0 || Nk == 0) return 0;
-  // enough for either partial pass: mha_fwd_paged (always the CUDA-core
-  // pass) takes its workspace size from this function too
+  // enough for either partial pass, so that the size does not depend on
+  // which pass a call takes
   return std::max(make_plan(BH, Nq, Nk, d, num_splits, true).total,
                   make_plan(BH, Nq, Nk, d, num_splits, false).total);
 }
@@ -183,6 +200,7 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
   const bool tensor = use_tensor_path(Nq, d);
   const Plan pl = make_plan(BH, Nq, Nk, d, num_splits, tensor);
   if (workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
+  if (BH * pl.splits > 0x7fffffffll) return MHA_ERR_INVALID_ARG;  // work tiles are counted in int
   const size_t qb = static_cast<size_t>(BH) * Nq * d * 2, kb = static_cast<size_t>(BH) * Nk * d * 2;
   const size_t lb = static_cast<size_t>(BH) * Nq * 4;
   // outputs and workspace must not overlap the inputs or each other
@@ -201,11 +219,11 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
   rc = setup(&dev, &status);
   if (rc != MHA_OK) return rc;
   float* o_part = static_cast<float*>(workspace);
-  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                             ((pl.o_part_bytes + 15) & ~static_cast<size_t>(15)));
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.lse_off);
+  int* counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + pl.counter_off);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (tensor) {
-    rc = fwd_split_partial(q, k, v, o_part, lse_part, static_cast<int>(BH), Nq, Nk, d, scale,
+    rc = fwd_split_partial(q, k, v, o_part, lse_part, counter, static_cast<int>(BH), Nq, Nk, d, scale,
                            causal != 0, pl.splits, pl.tiles_per_split, dev, status, st);
     if (rc != MHA_OK) return rc;
     return launch_merge(o_part, lse_part, o, lse, BH, Nq, d, pl.splits, st);
@@ -217,9 +235,8 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
 
   mha::SplitParams prm = {};
   prm.q = static_cast<const __nv_bfloat16*>(q);
-  prm.o_part = static_cast<float*>(workspace);
-  prm.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                          ((pl.o_part_bytes + 15) & ~static_cast<size_t>(15)));
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
   prm.status = status;
   prm.wait_limit = wait_limit();
   prm.Nq = Nq;
@@ -228,7 +245,7 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
   prm.tiles_per_split = pl.tiles_per_split;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.causal = causal ? 1 : 0;
-  return run_split<false>(mk, mv, prm, BH, d, pl, o, lse, static_cast<cudaStream_t>(stream));
+  return run_split<false>(mk, mv, prm, BH, d, pl, o, lse, st);
 }
 
 int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
@@ -251,8 +268,10 @@ int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const
       !aligned16(lse) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3))
     return MHA_ERR_MISALIGNED;
-  const Plan pl = make_plan(BH, Nq, static_cast<int>(max_keys), d, num_splits, false);
+  const bool tensor = use_tensor_path(Nq, d);
+  const Plan pl = make_plan(BH, Nq, static_cast<int>(max_keys), d, num_splits, tensor);
   if (workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
+  if (BH * pl.splits > 0x7fffffffll) return MHA_ERR_INVALID_ARG;  // work tiles are counted in int
   const size_t qb = static_cast<size_t>(BH) * Nq * d * 2;
   const size_t cb = static_cast<size_t>(num_blocks) * H * page_size * d * 2;
   const size_t lb = static_cast<size_t>(BH) * Nq * 4;
@@ -271,9 +290,26 @@ int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const
   unsigned* status = nullptr;
   rc = setup(&dev, &status);
   if (rc != MHA_OK) return rc;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.lse_off);
+  int* counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + pl.counter_off);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (tensor) {
+    rc = fwd_paged_partial(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, counter, B, H,
+                           Nq, d, page_size, num_blocks, max_blocks, scale, causal != 0, pl.splits,
+                           pl.tiles_per_split, dev, status, st);
+    if (rc != MHA_OK) return rc;
+    PagedSplits ps;
+    ps.seq_lens = seq_lens;
+    ps.num_heads = H;
+    ps.max_keys = static_cast<int>(max_keys);
+    ps.split_keys = static_cast<long long>(pl.tiles_per_split) * pl.tile_keys;
+    return launch_merge(o_part, lse_part, o, lse, BH, Nq, d, pl.splits, st, ps);
+  }
   CUtensorMap mk, mv;
-  if (!encode_paged_map(&mk, k_cache, num_blocks, H, page_size, d) ||
-      !encode_paged_map(&mv, v_cache, num_blocks, H, page_size, d))
+  const int rows = page_size < 64 ? page_size : 64;
+  if (!encode_paged_map(&mk, k_cache, num_blocks, H, page_size, d, rows) ||
+      !encode_paged_map(&mv, v_cache, num_blocks, H, page_size, d, rows))
     return MHA_ERR_CUDA;
   mha::SplitParams prm = {};
   prm.q = static_cast<const __nv_bfloat16*>(q);
@@ -282,9 +318,9 @@ int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const
   prm.page_size = page_size;
   prm.max_blocks = max_blocks;
   prm.num_heads = H;
-  prm.o_part = static_cast<float*>(workspace);
-  prm.lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) +
-                                          ((pl.o_part_bytes + 15) & ~static_cast<size_t>(15)));
+  prm.num_blocks = num_blocks;
+  prm.o_part = o_part;
+  prm.lse_part = lse_part;
   prm.status = status;
   prm.wait_limit = wait_limit();
   prm.Nq = Nq;
@@ -293,7 +329,7 @@ int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const
   prm.tiles_per_split = pl.tiles_per_split;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   prm.causal = causal ? 1 : 0;
-  return run_split<true>(mk, mv, prm, BH, d, pl, o, lse, static_cast<cudaStream_t>(stream));
+  return run_split<true>(mk, mv, prm, BH, d, pl, o, lse, st);
 }
 
 }  // extern "C"

@@ -35,7 +35,7 @@ struct SplitParams {
   // block_table[b * max_blocks + t / page_size], row t % page_size
   const int* block_table;  // [B, max_blocks]
   const int* seq_lens;     // [B] keys cached per batch entry
-  int page_size, max_blocks, num_heads;
+  int page_size, max_blocks, num_heads, num_blocks;
   float* o_part;           // [BH, splits, Nq, D]  (normalised by the split's own sum)
   float* lse_part;         // [BH, splits, Nq]     (natural log; -inf when empty)
   unsigned* status;        // device status word
@@ -70,16 +70,6 @@ struct SplitCfg {
                 "key-group combine buffer reuses the ring");
   static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
 };
-
-// 4-D TMA load (paged cache: x = d, y = row in page, z = head, w = block).
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int x, int y, int z, int w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
-}
 
 // Byte offset of element (row, col) of a [rows x 64] bf16 box written by TMA
 // with the 128-byte swizzle: 16-byte chunk index XOR (row mod 8).
@@ -119,32 +109,38 @@ __global__ void __launch_bounds__(SplitCfg<D, QB>::kThreads, 2)
   auto v_tile = [&](int i) -> uint32_t { return sbase + C::kOffRing + (2 * i + 1) * C::kTileBytes; };
   const WaitCtl ctl{abort_flag, p.status, p.wait_limit};
 
-  auto issue_tile = [&](int t) {  // thread 0 only
+  auto issue_tile = [&](int t) {  // warp 0, all lanes
     const int slot = t % C::kStages;
-    ptx::mbar_arrive_expect_tx(full(slot), 2 * C::kTileBytes);
+    if (lane == 0) ptx::mbar_arrive_expect_tx(full(slot), 2 * C::kTileBytes);
+    __syncwarp();
     const int y = (t_begin + t) * C::kTileKeys;
     if constexpr (PAGED) {
       // the tile's 64 keys come from one page (pages >= 64 keys) or from
-      // 64 / page_size consecutive pages; each box lands 1024-byte aligned,
-      // so the 128-byte swizzle of the whole tile stays as one box's
+      // 64 / page_size consecutive pages, lane r loading box r (so the
+      // table reads overlap); each box lands 1024-byte aligned, so the
+      // 128-byte swizzle of the whole tile stays as one box's
       const int rows = min(p.page_size, C::kTileKeys);
-      const int b = bh / p.num_heads, head = bh % p.num_heads;
-      for (int r0 = 0; r0 < C::kTileKeys; r0 += rows) {
+      if (lane < C::kTileKeys / rows) {
+        const int b = bh / p.num_heads, head = bh % p.num_heads;
+        const int r0 = lane * rows;
         const int pos = y + r0;
-        const int page = min(pos / p.page_size, p.max_blocks - 1);
-        const int blk = p.block_table[static_cast<size_t>(b) * p.max_blocks + page];
+        // pages past the entry's length: a block id past the cache reads as
+        // zeros (pos < Nk also keeps the table read inside its row)
+        const int blk = pos < Nk ? p.block_table[static_cast<size_t>(b) * p.max_blocks + pos / p.page_size]
+                                 : p.num_blocks;
         const int row = pos % p.page_size;
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_4d(k_tile(slot) + h * C::kHalfBytes + r0 * 128, &tmK, full(slot), h * 64, row, head, blk);
-          tma_load_4d(v_tile(slot) + h * C::kHalfBytes + r0 * 128, &tmV, full(slot), h * 64, row, head, blk);
+          ptx::tma_load_4d(k_tile(slot) + h * C::kHalfBytes + r0 * 128, &tmK, full(slot), h * 64, row, head, blk);
+          ptx::tma_load_4d(v_tile(slot) + h * C::kHalfBytes + r0 * 128, &tmV, full(slot), h * 64, row, head, blk);
         }
       }
-    } else {
+    } else if (lane == 0) {
       for (int h = 0; h < D / 64; ++h) {
         ptx::tma_load_3d(k_tile(slot) + h * C::kHalfBytes, &tmK, full(slot), h * 64, y, bh);
         ptx::tma_load_3d(v_tile(slot) + h * C::kHalfBytes, &tmV, full(slot), h * 64, y, bh);
       }
     }
+    __syncwarp();
   };
 
   if (tid == 0) {
@@ -160,7 +156,7 @@ __global__ void __launch_bounds__(SplitCfg<D, QB>::kThreads, 2)
     q_s[i] = qi < Nq ? __bfloat162float(p.q[(static_cast<size_t>(bh) * Nq + qi) * D + c]) : 0.f;
   }
   __syncthreads();
-  if (tid == 0)
+  if (warp == 0)
     for (int t = 0; t < min(n_tiles, C::kStages); ++t) issue_tile(t);
 
   // per-warp running statistics of queries w, w+4, w+8, w+12
@@ -190,6 +186,23 @@ __global__ void __launch_bounds__(SplitCfg<D, QB>::kThreads, 2)
     const int key0 = (t_begin + t) * C::kTileKeys;
     const uint8_t* kt = smem + (k_tile(slot) - sbase);
     const uint8_t* vt = smem + (v_tile(slot) - sbase);
+    if constexpr (PAGED) {
+      // V rows past the entry's length that came from its last, partly
+      // filled page hold whatever the cache holds there, possibly NaN, and
+      // a zero weight times NaN is NaN: clear them (the scores of those keys
+      // are masked by a select, so K needs no clearing).  The clear is
+      // ordered before the P V step by the barrier after the scores.
+      const int valid = Nk - key0;
+      if (valid < C::kTileKeys && valid % min(p.page_size, C::kTileKeys) != 0) {
+        const int n16 = (C::kTileKeys - valid) * 8;  // 16-byte pieces per half
+        uint8_t* vz = smem + (v_tile(slot) - sbase);
+        for (int i = tid; i < (D / 64) * n16; i += C::kThreads) {
+          const int h = i / n16, r = i - h * n16;
+          *reinterpret_cast<uint4*>(vz + h * C::kHalfBytes + valid * 128 + r * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        ptx::fence_proxy_async_smem();
+      }
+    }
     // ---- scores: two threads per key, each over half of d ----
     {
       const int kk = tid >> 1, half = tid & 1;
@@ -290,7 +303,7 @@ __global__ void __launch_bounds__(SplitCfg<D, QB>::kThreads, 2)
       }
     }
     __syncthreads();  // the slot is free again
-    if (tid == 0 && issued < n_tiles) {
+    if (warp == 0 && issued < n_tiles) {
       issue_tile(issued);
       ++issued;
     }
@@ -340,15 +353,24 @@ __global__ void __launch_bounds__(SplitCfg<D, QB>::kThreads, 2)
 template <int D>
 __global__ void __launch_bounds__(D) splitkv_merge_kernel(const float* o_part, const float* lse_part,
                                                          __nv_bfloat16* o, float* lse, int Nq,
-                                                         int num_splits) {
+                                                         int num_splits, const int* seq_lens,
+                                                         int num_heads, long long split_keys,
+                                                         int max_keys) {
   const int qi = blockIdx.x, bh = blockIdx.y, c = threadIdx.x;
   const size_t base = static_cast<size_t>(bh) * num_splits;
+  // paged caches: an entry has only the splits that hold some of its keys
+  // (the partial pass may skip the others and leave their slots unwritten)
+  int ns = num_splits;
+  if (seq_lens) {
+    const long long nk = max(0, min(seq_lens[bh / num_heads], max_keys));
+    ns = static_cast<int>(min(static_cast<long long>(num_splits), (nk + split_keys - 1) / split_keys));
+  }
   float lmax = -INFINITY;
-  for (int s = 0; s < num_splits; ++s) lmax = fmaxf(lmax, lse_part[(base + s) * Nq + qi]);
+  for (int s = 0; s < ns; ++s) lmax = fmaxf(lmax, lse_part[(base + s) * Nq + qi]);
   float out = 0.f, lse_row = -INFINITY;
   if (lmax != -INFINITY) {
     float wsum = 0.f, acc = 0.f;
-    for (int s = 0; s < num_splits; ++s) {
+    for (int s = 0; s < ns; ++s) {
       const float w = __expf(lse_part[(base + s) * Nq + qi] - lmax);
       wsum += w;
       acc = fmaf(w, o_part[((base + s) * Nq + qi) * D + c], acc);

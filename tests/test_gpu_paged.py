@@ -1,5 +1,7 @@
 """GPU parity of the paged-KV path: random block tables and per-sequence
-lengths, checked against the fp64 oracle on each sequence's gathered keys."""
+lengths, checked against the fp64 oracle on each sequence's gathered keys.
+Both partial passes are covered: the tensor-core one (d = 128, or three or
+more queries) and the CUDA-core one (d = 64 with one or two queries)."""
 import numpy as np
 import pytest
 
@@ -43,7 +45,7 @@ def gather(kc, table, b, n, page):
 
 @pytest.mark.parametrize("page", [16, 64, 128])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d,Nq", [(128, 1), (64, 4)])
+@pytest.mark.parametrize("d,Nq", [(128, 1), (64, 4), (64, 2)])
 def test_paged_against_oracle(page, causal, d, Nq):
     import torch
 
@@ -78,26 +80,32 @@ def test_paged_against_oracle(page, causal, d, Nq):
             (b, do.max(), do.mean(), dl.max())
 
 
-def test_paged_equals_contiguous_when_identity():
+@pytest.mark.parametrize("d,Nq,page", [(64, 2, 64), (128, 1, 64), (128, 4, 128), (64, 8, 16)])
+def test_paged_equals_contiguous_when_identity(d, Nq, page):
     """An identity block table over a cache laid out like [B*H...] gives the
-    same result, bit for bit, as the contiguous split-KV entry point when both
-    take the same partial pass (the CUDA-core one: d = 64 with two queries;
-    contiguous K/V at d = 128 go through the tensor cores instead)."""
+    same result, bit for bit, as the contiguous split-KV entry point: both
+    take the same partial pass (the CUDA-core one for d = 64 with two
+    queries, the tensor-core one otherwise) with the same splits, and the
+    600-key sequences end inside a page, where the paged pass clears the
+    rows past the end that the contiguous one reads as zeros."""
     import torch
 
     import head_attention_forward_gb300 as mha
-    B, H, Nq, d, page, n = 2, 2, 2, 64, 64, 640
-    mb = n // page
+    B, H, n = 2, 2, 600
+    mb = (n + page - 1) // page
     q = synth.normal_bf16(3, 0, B * H * Nq * d).reshape(B, H, Nq, d)
     k = synth.normal_bf16(3, 1, B * H * n * d).reshape(B, H, n, d)
     v = synth.normal_bf16(3, 2, B * H * n * d).reshape(B, H, n, d)
+    pad = np.zeros((B, H, mb * page - n, d), dtype=k.dtype)
+    kp, vp = np.concatenate([k, pad], axis=2), np.concatenate([v, pad], axis=2)
     # cache block (b * mb + i) holds keys i*page.. of entry b, all heads
-    kc = np.ascontiguousarray(k.reshape(B, H, mb, page, d).transpose(0, 2, 1, 3, 4).reshape(B * mb, H, page, d))
-    vc = np.ascontiguousarray(v.reshape(B, H, mb, page, d).transpose(0, 2, 1, 3, 4).reshape(B * mb, H, page, d))
+    kc = np.ascontiguousarray(kp.reshape(B, H, mb, page, d).transpose(0, 2, 1, 3, 4).reshape(B * mb, H, page, d))
+    vc = np.ascontiguousarray(vp.reshape(B, H, mb, page, d).transpose(0, 2, 1, 3, 4).reshape(B * mb, H, page, d))
     table = np.arange(B * mb, dtype=np.int32).reshape(B, mb)
     seq = np.full(B, n, dtype=np.int32)
     scale = scale_for(d)
-    ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, n, d, 3)
+    ws_bytes = max(mha.mha_fwd_kv_workspace_size(B, H, Nq, n, d, 3),
+                   mha.mha_fwd_kv_workspace_size(B, H, Nq, mb * page, d, 3))
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     o1 = torch.empty((B, H, Nq, d), dtype=torch.bfloat16, device="cuda")
     l1 = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
@@ -108,8 +116,62 @@ def test_paged_equals_contiguous_when_identity():
     l2 = torch.empty_like(l1)
     mha.mha_fwd_kv(to_device(q), to_device(k), to_device(v), o2, l2, B, H, Nq, n, d, scale, True, 3,
                    ws, ws_bytes)
-    torch.cuda.synchronize()
+    rc, word = mha.mha_device_status()
+    assert rc == mha.MHA_OK, f"status {word:#x}"
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+@pytest.mark.parametrize("page", [16, 64, 256])
+@pytest.mark.parametrize("d,Nq,causal", [(128, 1, False), (128, 2, True), (64, 1, False), (64, 2, True)])
+def test_paged_nan_outside_sequences(page, d, Nq, causal):
+    """Every cache row outside the sequences' keys holds NaN: the rest of
+    each sequence's last page, the unused pages, and the rows the table
+    entries past each length point at.  None of it may reach O or LSE.  A
+    zero-length sequence gives O = 0 and LSE = -inf."""
+    import torch
+
+    import head_attention_forward_gb300 as mha
+    B, H = 4, 2
+    max_blocks = (700 + page - 1) // page + 1
+    seq = np.array([0, 1, 333, 700], dtype=np.int32)
+    q, kc, vc, table, nb = make_paged(90 + page + d, B, H, Nq, d, page, max_blocks, seq)
+    nan = np.uint16(0x7FC0)  # bf16 quiet NaN
+    live = np.zeros((nb, page), dtype=bool)
+    for b in range(B):
+        for t in range(int(seq[b])):
+            live[table[b, t // page], t % page] = True
+    kn, vn = kc.copy(), vc.copy()
+    kn[~live[:, None, :].repeat(H, axis=1)] = nan
+    vn[~live[:, None, :].repeat(H, axis=1)] = nan
+    # table entries past each length point at real (NaN-filled) blocks
+    spare = [blk for blk in range(nb) if not live[blk].any()]
+    for b in range(B):
+        used = (int(seq[b]) + page - 1) // page
+        for i in range(used, max_blocks):
+            table[b, i] = spare[(b + i) % len(spare)]
+    scale = scale_for(d)
+    o = torch.full((B, H, Nq, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((B, H, Nq), float("nan"), dtype=torch.float32, device="cuda")
+    ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, max_blocks * page, d, 0)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    mha.mha_fwd_paged(to_device(q), to_device(kn), to_device(vn), torch.from_numpy(table).cuda(),
+                      torch.from_numpy(seq).cuda(), o, lse, B, H, Nq, d, page, nb, max_blocks, scale,
+                      causal, 0, ws, ws_bytes)
+    rc, word = mha.mha_device_status()
+    assert rc == mha.MHA_OK, f"status {word:#x}"
+    og, lg = bf16_to_f64(o), lse.cpu().numpy().astype(np.float64)
+    assert np.all(og[0] == 0) and np.all(np.isneginf(lg[0]))
+    assert np.isfinite(og).all()
+    for b in range(1, B):
+        n = int(seq[b])
+        kb, vb = gather(kc, table, b, n, page), gather(vc, table, b, n, page)
+        o_ref, l_ref = oracle.attention_kv(q[b:b + 1], kb[None], vb[None], scale, causal)
+        empty = np.isneginf(l_ref[0])
+        assert np.array_equal(np.isneginf(lg[b]), empty)
+        do = np.abs(og[b] - o_ref[0])
+        dl = np.abs(lg[b][~empty] - l_ref[0][~empty]) if (~empty).any() else np.zeros(1)
+        assert do.max() <= TOL_MAX_O and do.mean() <= TOL_MEAN_O and dl.max() <= TOL_MAX_LSE, \
+            (b, do.max(), do.mean(), dl.max())
 
 
 def gather_or_zero(kc, table, b, n, page, num_blocks):

@@ -80,7 +80,6 @@ def load_peaks():
 # valid only while these are unchanged.
 KERNEL_SOURCES = {
     "mha_fwd_kernel": ("mha_fwd_kernel.cuh", "sm103_ptx.cuh", "mha_wait.cuh"),
-    "splitkv_partial_kernel": ("mha_splitkv_kernel.cuh", "sm103_ptx.cuh", "mha_wait.cuh"),
 }
 
 
@@ -314,9 +313,7 @@ def run_decode(args, name):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": gbs / hbm_peak, "traffic": recorded_traffic(name),
                      "algorithmic_bytes_per_step": algo_bytes,
-                     "kernel": (f"mha_fwd_kernel<{d},{int(bool(causal))},split> + splitkv_merge_kernel<{d}>"
-                                if (d == 128 or Nq >= 3) else  # the library's choice of partial pass
-                                f"splitkv_partial_kernel<{d}> + splitkv_merge_kernel<{d}>")},
+                     "kernel": f"mha_fwd_kernel<{d},{int(bool(causal))},split> + splitkv_merge_kernel<{d}>"},
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }
@@ -391,9 +388,7 @@ def run_paged(args, name):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": src, "traffic": recorded_traffic(name),
                      "algorithmic_bytes_per_step": algo_bytes,
-                     "kernel": (f"mha_fwd_kernel<{d},{int(bool(causal))},split,paged> + splitkv_merge_kernel<{d}>"
-                                if (d == 128 or Nq >= 3) else  # the library's choice of partial pass
-                                f"splitkv_partial_kernel<{d},paged> + splitkv_merge_kernel<{d}>")},
+                     "kernel": f"mha_fwd_kernel<{d},{int(bool(causal))},split,paged> + splitkv_merge_kernel<{d}>"},
         "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
     }), flush=True)
     return 0

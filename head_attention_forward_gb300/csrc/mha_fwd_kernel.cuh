@@ -252,9 +252,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       ptx::mbar_init(kv_full(i), 1);
       ptx::mbar_init(kv_empty(i), 1);
     }
+    // one elected arrive per softmax warp of the stage; split mode: per
+    // warp that holds one of the Nq query rows (the others sit idle)
+    const int p_arrivals = SPLIT ? min(4, (p.Nq + 31) / 32) : 4;
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(s_full(s), 1);
-      ptx::mbar_init(p_ready(s), 4);  // one elected arrive per softmax warp
+      ptx::mbar_init(p_ready(s), p_arrivals);
       ptx::mbar_init(o_full(s), 1);
     }
     ptx::mbar_init(drain_bar, 1);
@@ -507,11 +510,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         __syncwarp();
       };
-      // O(s) += P(s) V over 128 keys in steps of 16; P read from TMEM
-      auto issue_pv = [&](int s, int vslot, bool first) {
+      // O(so) += P V over 128 keys in steps of 16; P read from TMEM, from
+      // the S columns of stage sp
+      auto issue_pv_from = [&](int sp, int so, int vslot, bool first) {
         const uint64_t dv = dV0 + slot_off(vslot);
-        const uint32_t ts = s ? tS1 : tS0;
-        const uint32_t to = s ? tO1 : tO0;
+        const uint32_t ts = sp ? tS1 : tS0;
+        const uint32_t to = so ? tO1 : tO0;
         if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < C::kBlockN / 16; ++kk)
@@ -520,6 +524,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         }
         __syncwarp();
       };
+      auto issue_pv = [&](int s, int vslot, bool first) { issue_pv_from(s, s, vslot, first); };
       auto commit = [&](uint32_t b) {
         if (ptx::elect_one()) ptx::mma_commit(b);
         __syncwarp();
@@ -536,6 +541,42 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         const int qb = q_set(kq);
         if (!(ok = wait_warp(q_full(qb), q_par(kq), ctl, kSiteMmaQ))) break;
         ++kq;
+        if constexpr (SPLIT) {
+          // One stage, its scores double-buffered in the S columns of both
+          // stages: S_{j+1} = Q K_{j+1}^T is issued before P_j V_j, so the
+          // softmax of tile j+1 starts as soon as that of tile j is done
+          // instead of waiting for P_j V_j and then S_{j+1}.  (The MMAs run
+          // in issue order, so S_{j+2} overwrites P_j only after P_j V_j.)
+          // o_full(0) completes after every P_j V_j: the softmax, whose
+          // rescale of O may otherwise meet P_{j-1} V_{j-1} still running,
+          // waits on it at every tile after the first and at the epilogue.
+          const int n = tl.n0;
+          const int t0 = t;  // ring position of K_0
+          auto slot_of = [&](int pos) { return pos % C::kStages; };
+          auto par_of = [&](int pos) { return static_cast<uint32_t>((pos / C::kStages) & 1); };
+          for (int j = -1; j < n && ok; ++j) {
+            if (j + 1 < n) {
+              const int kp = t0 + 2 * (j + 1);  // K_{j+1}
+              if (!(ok = wait_warp(kv_full(slot_of(kp)), par_of(kp), ctl, kSiteMmaKV))) break;
+              ptx::tc_fence_after();
+              issue_s(qb, (j + 1) & 1, slot_of(kp));
+              commit(s_full((j + 1) & 1));
+              commit(kv_empty(slot_of(kp)));
+              if (j + 2 == n) commit(q_empty(qb));  // this tile's Q is no longer read
+            }
+            if (j < 0) continue;
+            const int vp = t0 + 2 * j + 1;  // V_j
+            if (!(ok = wait_warp(p_ready(0), pr[0] & 1, ctl, kSiteMmaP))) break;
+            ++pr[0];
+            if (!(ok = wait_warp(kv_full(slot_of(vp)), par_of(vp), ctl, kSiteMmaKV))) break;
+            ptx::tc_fence_after();
+            issue_pv_from(j & 1, 0, slot_of(vp), j == 0);
+            commit(o_full(0));
+            commit(kv_empty(slot_of(vp)));
+          }
+          t = t0 + 2 * n;
+          continue;
+        }
         int v_prev = 0;
         for (int j = 0; j < n_kv && ok; ++j) {
           const int k_slot = t % C::kStages, k_par = (t / C::kStages) & 1;
@@ -591,25 +632,33 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t t_o = tmem + lane_off + (s ? C::kColO1 : C::kColO0);
     const float sl2 = p.scale_log2;
     bool ok = true;
-    int sf = 0;  // s_full completions consumed
+    int sf[2] = {0, 0};  // s_full completions consumed, per S buffer
     int of = 0;  // o_full completions consumed
     Tile tl;
+    // split mode: a warp whose 32 rows all lie past the Nq queries has no
+    // work, and leaves its SM sub-partition to the warps that share it
+    // (the K/V producer, the MMA issuer, the Q producer)
+    const bool idle = SPLIT && wq * 32 >= p.Nq;
     for (int k = 0; ok && take_tile(k, tl, ok, true, kSiteSoftmaxS); ++k) {
       const int m0 = tl.m0;
-      const int n = s ? tl.n1 : tl.n0;
+      const int n = idle ? 0 : (s ? tl.n1 : tl.n0);
       const int q_idx = m0 + s * C::kBlockM + row;
       float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale
       float l_run = 0.f;   // row sum of exp2 terms (fp32), for the LSE
       float lr_run = 0.f;  // the same over the bf16-rounded terms, for O
       for (int j = 0; j < n; ++j) {
-        if (!wait_warp(s_full(s), sf & 1, ctl, kSiteSoftmaxS)) {
+        // S buffer of this tile: the stage's own, or in split mode the two
+        // stages' S columns in turn
+        const int sb = SPLIT ? (j & 1) : s;
+        const uint32_t t_sj = SPLIT ? tmem + lane_off + (sb ? C::kColS1 : C::kColS0) : t_s;
+        if (!wait_warp(s_full(sb), sf[sb] & 1, ctl, kSiteSoftmaxS)) {
           ok = false;
           break;
         }
-        ++sf;
+        ++sf[sb];
         ptx::tc_fence_after();
         uint32_t raw[128];
-        ptx::tmem_ld_x128(t_s, raw);
+        ptx::tmem_ld_x128(t_sj, raw);
         float x[128];
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc) x[cc] = __uint_as_float(raw[cc]);
@@ -660,10 +709,19 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             sumr[(2 * i) & 3] = ptx::add_bf16_lo(pk[i], sumr[(2 * i) & 3]);
             sumr[(2 * i + 1) & 3] = ptx::add_bf16_hi(pk[i], sumr[(2 * i + 1) & 3]);
           }
-          ptx::tmem_st_x16(t_s + c4 * 16, pk);
+          ptx::tmem_st_x16(t_sj + c4 * 16, pk);
         }
         l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
         lr_run = lr_run * alpha + ((sumr[0] + sumr[1]) + (sumr[2] + sumr[3]));
+        if (SPLIT && j > 0) {
+          // P_{j-1} V_{j-1} was issued after S_j: it lands before O is touched
+          if (!wait_warp(o_full(0), of & 1, ctl, kSiteSoftmaxO)) {
+            ok = false;
+            break;
+          }
+          ++of;
+          ptx::tc_fence_after();
+        }
         // correction: bring O(s) to the new max before P_j(s) V_j lands on it
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll

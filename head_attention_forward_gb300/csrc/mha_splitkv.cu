@@ -1,12 +1,11 @@
 // mha_splitkv.cu - host side of the split-KV attention forward (a few
-// queries against a long key/value sequence): argument checks, workspace
-// layout, split count, TMA maps and the two launches.
+// queries against a long key/value sequence, contiguous or paged): argument
+// checks, split count, workspace layout, and the partial + merge launches.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
-#include <mutex>
-#include <type_traits>
 
 #include "mha_fwd.h"
 #include "mha_internal.h"
@@ -16,50 +15,33 @@ namespace {
 
 using namespace mha_host;
 
-constexpr int kMaxDevices = 64;
-// Target CTA count when the caller lets the library pick the split count:
-// four waves of two CTAs per SM on a 152-SM part.  A fixed constant keeps the
-// workspace size a pure function of the problem shape.
-constexpr int kTargetCtas = 4 * 2 * 152;
-// The tensor-core partial pass (the persistent attention kernel in split
-// mode, one CTA per SM) takes 128-key tiles and hands (head, split) work
-// tiles out at run time.  Each work tile costs a pipeline drain at its end,
-// so fewer, longer ones do better until the last ones leave CTAs idle:
-// about six per CTA measured best on decode shapes (88-98% of the HBM copy
-// rate against 84-88% with 32 per CTA).
+// The partial pass (the persistent attention kernel in split mode, one CTA
+// per SM) takes 128-key tiles and hands (head, split) work tiles out at run
+// time.  Each work tile costs a pipeline drain at its end, so fewer, longer
+// ones do better until the last ones leave CTAs idle: about six per CTA
+// measured best on decode shapes (88-98% of the HBM copy rate against
+// 84-88% with 32 per CTA).  A fixed constant keeps the workspace size a
+// pure function of the problem shape.
+constexpr int kTileKeys = 128;
 constexpr int kTargetTiles = 6 * 152;
-// K/V (contiguous or paged) go through the tensor-core pass at d = 128
-// always, and at d = 64 from three queries on.  The CUDA-core kernel re-reads Q from shared
-// memory for every key, so it falls behind as queries are added; at d = 64
-// with one or two queries it still streams faster (76% vs 55% of HBM
-// bandwidth for one query, measured), because there the tensor-core pass is
-// bound by its softmax rather than by HBM.
-bool use_tensor_path(int Nq, int d) { return d == 128 || Nq >= 3; }
-
-std::mutex g_mu;
-bool g_attr_done[kMaxDevices] = {};
 
 struct Plan {
-  int splits = 0, tiles_per_split = 0, tile_keys = 0;
+  int splits = 0, tiles_per_split = 0;
   size_t o_part_bytes = 0, lse_part_bytes = 0, lse_off = 0, counter_off = 0, total = 0;
 };
 
 // Split count and workspace layout: o_part fp32 [BH, splits, Nq, d], then
 // (16-byte aligned) lse_part fp32 [BH, splits, Nq], then (16-byte aligned)
-// the tensor-core pass's work-tile counter (one int in 16 bytes).  Splits
-// are runs of 64-key tiles (CUDA-core pass) or 128-key tiles (tensor-core
-// pass).
-Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits, bool tensor) {
+// the partial pass's work-tile counter (one int in 16 bytes).  A split is a
+// run of tiles_per_split 128-key tiles.
+Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits) {
   Plan pl;
-  const int tile_keys = tensor ? 128 : 64;
-  const int target = tensor ? kTargetTiles : kTargetCtas;
-  const int tiles = (Nk + tile_keys - 1) / tile_keys;
+  const int tiles = (Nk + kTileKeys - 1) / kTileKeys;
   int want = num_splits > 0 ? num_splits
-                            : static_cast<int>(std::max<long long>(1, (target + BH - 1) / BH));
+                            : static_cast<int>(std::max<long long>(1, (kTargetTiles + BH - 1) / BH));
   want = std::max(1, std::min(want, tiles));
   pl.tiles_per_split = (tiles + want - 1) / want;
   pl.splits = (tiles + pl.tiles_per_split - 1) / pl.tiles_per_split;
-  pl.tile_keys = tile_keys;
   pl.o_part_bytes = static_cast<size_t>(BH) * pl.splits * Nq * d * 4;
   pl.lse_part_bytes = static_cast<size_t>(BH) * pl.splits * Nq * 4;
   pl.lse_off = (pl.o_part_bytes + 15) & ~static_cast<size_t>(15);
@@ -74,39 +56,6 @@ int check_shape(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (Nq > mha::kSplitMaxQ) return MHA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * H > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
   return MHA_OK;
-}
-
-template <int V>
-using Int = std::integral_constant<int, V>;
-
-// Calls f(Int<D>, Int<QB>) for every compiled partial-kernel variant.
-template <typename F>
-void for_each_variant(F&& f) {
-  f(Int<64>(), Int<1>()); f(Int<64>(), Int<2>()); f(Int<64>(), Int<4>());
-  f(Int<64>(), Int<8>()); f(Int<64>(), Int<16>());
-  f(Int<128>(), Int<1>()); f(Int<128>(), Int<2>()); f(Int<128>(), Int<4>());
-  f(Int<128>(), Int<8>()); f(Int<128>(), Int<16>());
-}
-
-int query_bucket(int Nq) { return Nq <= 1 ? 1 : Nq <= 2 ? 2 : Nq <= 4 ? 4 : Nq <= 8 ? 8 : 16; }
-
-template <int D, int QB, bool PAGED>
-cudaError_t launch_partial(cudaLaunchConfig_t cfg, const CUtensorMap& mk, const CUtensorMap& mv,
-                           const mha::SplitParams& prm) {
-  cfg.dynamicSmemBytes = mha::SplitCfg<D, QB>::kSmemBytes;
-  return cudaLaunchKernelEx(&cfg, mha::splitkv_partial_kernel<D, QB, PAGED>, mk, mv, prm);
-}
-
-template <int D, bool PAGED>
-cudaError_t launch_partial_d(cudaLaunchConfig_t cfg, const CUtensorMap& mk, const CUtensorMap& mv,
-                             const mha::SplitParams& prm) {
-  switch (query_bucket(prm.Nq)) {
-    case 1: return launch_partial<D, 1, PAGED>(cfg, mk, mv, prm);
-    case 2: return launch_partial<D, 2, PAGED>(cfg, mk, mv, prm);
-    case 4: return launch_partial<D, 4, PAGED>(cfg, mk, mv, prm);
-    case 8: return launch_partial<D, 8, PAGED>(cfg, mk, mv, prm);
-    default: return launch_partial<D, 16, PAGED>(cfg, mk, mv, prm);
-  }
 }
 
 // Paged caches: what the merge needs to count each entry's splits.
@@ -134,42 +83,6 @@ int launch_merge(const float* o_part, const float* lse_part, void* o, float* lse
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
-// Partial kernel + merge kernel on `stream` (shared by the contiguous and
-// the paged entry points).
-template <bool PAGED>
-int run_split(const CUtensorMap& mk, const CUtensorMap& mv, mha::SplitParams prm, long long BH,
-              int d, const Plan& pl, void* o, float* lse, cudaStream_t st) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(pl.splits), static_cast<unsigned>(BH), 1);
-  cfg.blockDim = dim3(128, 1, 1);
-  cfg.stream = st;
-  cudaError_t err = d == 64 ? launch_partial_d<64, PAGED>(cfg, mk, mv, prm)
-                            : launch_partial_d<128, PAGED>(cfg, mk, mv, prm);
-  if (err != cudaSuccess) return MHA_ERR_CUDA;
-  return launch_merge(prm.o_part, prm.lse_part, o, lse, BH, prm.Nq, d, pl.splits, st);
-}
-
-int setup(int* dev, unsigned** status) {
-  const int rc = device_setup(dev, status);
-  if (rc != MHA_OK) return rc;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_attr_done[*dev]) {
-    bool fail = false;
-    for_each_variant([&](auto d_tag, auto q_tag) {
-      constexpr int D = decltype(d_tag)::value, QB = decltype(q_tag)::value;
-      fail |= cudaFuncSetAttribute(mha::splitkv_partial_kernel<D, QB, false>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   mha::SplitCfg<D, QB>::kSmemBytes) != cudaSuccess;
-      fail |= cudaFuncSetAttribute(mha::splitkv_partial_kernel<D, QB, true>,
-                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   mha::SplitCfg<D, QB>::kSmemBytes) != cudaSuccess;
-    });
-    if (fail) return MHA_ERR_CUDA;
-    g_attr_done[*dev] = true;
-  }
-  return MHA_OK;
-}
-
 }  // namespace
 
 extern "C" {
@@ -178,10 +91,7 @@ size_t mha_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_sp
   if (check_shape(B, H, Nq, Nk, d, num_splits) != MHA_OK) return 0;
   const long long BH = static_cast<long long>(B) * H;
   if (BH == 0 || Nq == 0 || Nk == 0) return 0;
-  // enough for either partial pass, so that the size does not depend on
-  // which pass a call takes
-  return std::max(make_plan(BH, Nq, Nk, d, num_splits, true).total,
-                  make_plan(BH, Nq, Nk, d, num_splits, false).total);
+  return make_plan(BH, Nq, Nk, d, num_splits).total;
 }
 
 int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -197,8 +107,7 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) ||
       !aligned16(workspace))
     return MHA_ERR_MISALIGNED;
-  const bool tensor = use_tensor_path(Nq, d);
-  const Plan pl = make_plan(BH, Nq, Nk, d, num_splits, tensor);
+  const Plan pl = make_plan(BH, Nq, Nk, d, num_splits);
   if (workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
   if (BH * pl.splits > 0x7fffffffll) return MHA_ERR_INVALID_ARG;  // work tiles are counted in int
   const size_t qb = static_cast<size_t>(BH) * Nq * d * 2, kb = static_cast<size_t>(BH) * Nk * d * 2;
@@ -216,36 +125,16 @@ int mha_fwd_kv(const void* q, const void* k, const void* v, void* o, float* lse,
 
   int dev = 0;
   unsigned* status = nullptr;
-  rc = setup(&dev, &status);
+  rc = device_setup(&dev, &status);
   if (rc != MHA_OK) return rc;
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.lse_off);
   int* counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + pl.counter_off);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (tensor) {
-    rc = fwd_split_partial(q, k, v, o_part, lse_part, counter, static_cast<int>(BH), Nq, Nk, d, scale,
-                           causal != 0, pl.splits, pl.tiles_per_split, dev, status, st);
-    if (rc != MHA_OK) return rc;
-    return launch_merge(o_part, lse_part, o, lse, BH, Nq, d, pl.splits, st);
-  }
-  CUtensorMap mk, mv;
-  if (!encode_map(&mk, k, static_cast<int>(BH), Nk, d, 64) ||
-      !encode_map(&mv, v, static_cast<int>(BH), Nk, d, 64))
-    return MHA_ERR_CUDA;
-
-  mha::SplitParams prm = {};
-  prm.q = static_cast<const __nv_bfloat16*>(q);
-  prm.o_part = o_part;
-  prm.lse_part = lse_part;
-  prm.status = status;
-  prm.wait_limit = wait_limit();
-  prm.Nq = Nq;
-  prm.Nk = Nk;
-  prm.num_splits = pl.splits;
-  prm.tiles_per_split = pl.tiles_per_split;
-  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  prm.causal = causal ? 1 : 0;
-  return run_split<false>(mk, mv, prm, BH, d, pl, o, lse, st);
+  rc = fwd_split_partial(q, k, v, o_part, lse_part, counter, static_cast<int>(BH), Nq, Nk, d, scale,
+                         causal != 0, pl.splits, pl.tiles_per_split, dev, status, st);
+  if (rc != MHA_OK) return rc;
+  return launch_merge(o_part, lse_part, o, lse, BH, Nq, d, pl.splits, st);
 }
 
 int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const int* block_table,
@@ -268,8 +157,7 @@ int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const
       !aligned16(lse) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(block_table) & 3) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3))
     return MHA_ERR_MISALIGNED;
-  const bool tensor = use_tensor_path(Nq, d);
-  const Plan pl = make_plan(BH, Nq, static_cast<int>(max_keys), d, num_splits, tensor);
+  const Plan pl = make_plan(BH, Nq, static_cast<int>(max_keys), d, num_splits);
   if (workspace_bytes < pl.total) return MHA_ERR_INVALID_ARG;
   if (BH * pl.splits > 0x7fffffffll) return MHA_ERR_INVALID_ARG;  // work tiles are counted in int
   const size_t qb = static_cast<size_t>(BH) * Nq * d * 2;
@@ -288,48 +176,22 @@ int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const
 
   int dev = 0;
   unsigned* status = nullptr;
-  rc = setup(&dev, &status);
+  rc = device_setup(&dev, &status);
   if (rc != MHA_OK) return rc;
   float* o_part = static_cast<float*>(workspace);
   float* lse_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + pl.lse_off);
   int* counter = reinterpret_cast<int*>(static_cast<char*>(workspace) + pl.counter_off);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (tensor) {
-    rc = fwd_paged_partial(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, counter, B, H,
-                           Nq, d, page_size, num_blocks, max_blocks, scale, causal != 0, pl.splits,
-                           pl.tiles_per_split, dev, status, st);
-    if (rc != MHA_OK) return rc;
-    PagedSplits ps;
-    ps.seq_lens = seq_lens;
-    ps.num_heads = H;
-    ps.max_keys = static_cast<int>(max_keys);
-    ps.split_keys = static_cast<long long>(pl.tiles_per_split) * pl.tile_keys;
-    return launch_merge(o_part, lse_part, o, lse, BH, Nq, d, pl.splits, st, ps);
-  }
-  CUtensorMap mk, mv;
-  const int rows = page_size < 64 ? page_size : 64;
-  if (!encode_paged_map(&mk, k_cache, num_blocks, H, page_size, d, rows) ||
-      !encode_paged_map(&mv, v_cache, num_blocks, H, page_size, d, rows))
-    return MHA_ERR_CUDA;
-  mha::SplitParams prm = {};
-  prm.q = static_cast<const __nv_bfloat16*>(q);
-  prm.block_table = block_table;
-  prm.seq_lens = seq_lens;
-  prm.page_size = page_size;
-  prm.max_blocks = max_blocks;
-  prm.num_heads = H;
-  prm.num_blocks = num_blocks;
-  prm.o_part = o_part;
-  prm.lse_part = lse_part;
-  prm.status = status;
-  prm.wait_limit = wait_limit();
-  prm.Nq = Nq;
-  prm.Nk = static_cast<int>(max_keys);
-  prm.num_splits = pl.splits;
-  prm.tiles_per_split = pl.tiles_per_split;
-  prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  prm.causal = causal ? 1 : 0;
-  return run_split<true>(mk, mv, prm, BH, d, pl, o, lse, st);
+  rc = fwd_paged_partial(q, k_cache, v_cache, block_table, seq_lens, o_part, lse_part, counter, B, H, Nq,
+                         d, page_size, num_blocks, max_blocks, scale, causal != 0, pl.splits,
+                         pl.tiles_per_split, dev, status, st);
+  if (rc != MHA_OK) return rc;
+  PagedSplits ps;
+  ps.seq_lens = seq_lens;
+  ps.num_heads = H;
+  ps.max_keys = static_cast<int>(max_keys);
+  ps.split_keys = static_cast<long long>(pl.tiles_per_split) * kTileKeys;
+  return launch_merge(o_part, lse_part, o, lse, BH, Nq, d, pl.splits, st, ps);
 }
 
 }  // extern "C"

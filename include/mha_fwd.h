@@ -91,9 +91,8 @@ int mha_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  *             aligned, at least mha_fwd_kv_workspace_size(...) bytes, not
  *             overlapping any other argument.  Its contents need no
  *             initialisation and are garbage afterwards.
- *   stream  : cudaStream_t; two kernels are queued on it, preceded (when
- *             the tensor-core partial pass runs: d = 128, or Nq >= 3) by a
- *             4-byte memset of a work-tile counter in the workspace.
+ *   stream  : cudaStream_t; a 4-byte memset (of a work-tile counter in
+ *             the workspace) and two kernels are queued on it.
  *
  * B*H == 0 or Nq == 0 is a no-op.  Errors as for mha_fwd.
  */

@@ -1,7 +1,5 @@
 """GPU parity of the paged-KV path: random block tables and per-sequence
-lengths, checked against the fp64 oracle on each sequence's gathered keys.
-Both partial passes are covered: the tensor-core one (d = 128, or three or
-more queries) and the CUDA-core one (d = 64 with one or two queries)."""
+lengths, checked against the fp64 oracle on each sequence's gathered keys."""
 import numpy as np
 import pytest
 
@@ -84,10 +82,9 @@ def test_paged_against_oracle(page, causal, d, Nq):
 def test_paged_equals_contiguous_when_identity(d, Nq, page):
     """An identity block table over a cache laid out like [B*H...] gives the
     same result, bit for bit, as the contiguous split-KV entry point: both
-    take the same partial pass (the CUDA-core one for d = 64 with two
-    queries, the tensor-core one otherwise) with the same splits, and the
-    600-key sequences end inside a page, where the paged pass clears the
-    rows past the end that the contiguous one reads as zeros."""
+    run the same partial pass with the same splits, and the 600-key
+    sequences end inside a page, where the paged pass clears the rows past
+    the end that the contiguous one reads as zeros."""
     import torch
 
     import head_attention_forward_gb300 as mha

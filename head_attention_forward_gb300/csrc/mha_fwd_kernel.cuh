@@ -95,9 +95,8 @@ struct FwdCfg {
   static constexpr int kOffKV = kQSets * 2 * kTileBytes;
   static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
   // split mode: ring of work-tile ids from the K/V producer to the other
-  // roles (Q producer, MMA issuer, eight softmax warps)
+  // roles (Q producer, MMA issuer, the softmax warps that hold query rows)
   static constexpr int kTileRing = 8;
-  static constexpr int kTileConsumers = 1 + 1 + 8;
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_ready[2] o_full[2] drain
   // tail (paged mode: the copy of a V tile whose last rows get cleared)
   // tile_full[R] tile_empty[R]
@@ -253,7 +252,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       ptx::mbar_init(kv_empty(i), 1);
     }
     // one elected arrive per softmax warp of the stage; split mode: per
-    // warp that holds one of the Nq query rows (the others sit idle)
+    // warp of stage 0 that holds one of the Nq query rows (the other softmax
+    // warps have no work there and wait at the final barrier)
     const int p_arrivals = SPLIT ? min(4, (p.Nq + 31) / 32) : 4;
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(s_full(s), 1);
@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     ptx::mbar_init(tail_bar, 1);
     for (int i = 0; i < C::kTileRing; ++i) {
       ptx::mbar_init(tile_full(i), 1);
-      ptx::mbar_init(tile_empty(i), C::kTileConsumers);  // one arrive per consumer warp
+      ptx::mbar_init(tile_empty(i), 2 + p_arrivals);  // one arrive per consumer warp
     }
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -635,13 +635,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     int sf[2] = {0, 0};  // s_full completions consumed, per S buffer
     int of = 0;  // o_full completions consumed
     Tile tl;
-    // split mode: a warp whose 32 rows all lie past the Nq queries has no
-    // work, and leaves its SM sub-partition to the warps that share it
-    // (the K/V producer, the MMA issuer, the Q producer)
-    const bool idle = SPLIT && wq * 32 >= p.Nq;
-    for (int k = 0; ok && take_tile(k, tl, ok, true, kSiteSoftmaxS); ++k) {
+    // split mode: stage 1, and every warp whose 32 rows all lie past the
+    // Nq queries, has no work; such warps go straight to the final barrier
+    // (not even polling the tile ring), which leaves their SM
+    // sub-partitions to the warps that share them
+    const bool idle = SPLIT && (s == 1 || wq * 32 >= p.Nq);
+    for (int k = 0; !idle && ok && take_tile(k, tl, ok, true, kSiteSoftmaxS); ++k) {
       const int m0 = tl.m0;
-      const int n = idle ? 0 : (s ? tl.n1 : tl.n0);
+      const int n = s ? tl.n1 : tl.n0;
       const int q_idx = m0 + s * C::kBlockM + row;
       float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale
       float l_run = 0.f;   // row sum of exp2 terms (fp32), for the LSE

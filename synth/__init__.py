@@ -195,6 +195,7 @@ def decode_inputs(name: str, compiled: bool = True):
 # Paged-cache decode workloads: B sequences whose lengths spread between
 # lo and hi keys, pages of `page` keys scattered over the cache.
 PAGED_CONFIGS = {
+    "pag0": dict(B=8, H=32, Nq=1, d=128, page=64, lo=2048, hi=16384, causal=False, seed=11),  # ~1.2 GB: profiling size
     "pag1": dict(B=32, H=32, Nq=1, d=128, page=16, lo=2048, hi=16384, causal=False, seed=8),
     "pag2": dict(B=32, H=32, Nq=1, d=128, page=64, lo=2048, hi=16384, causal=False, seed=9),
 }

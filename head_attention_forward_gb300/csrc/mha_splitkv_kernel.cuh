@@ -21,14 +21,22 @@ namespace mha {
 constexpr int kSplitMaxQ = 16;  // queries per call (decode-sized blocks)
 
 // Merge of the split partials: one block per (query, batch*head), one thread
-// per output column.
+// per output column.  The splits' LSEs are read in parallel (thread t takes
+// splits t, t + D, ...) and their weights staged in shared memory D at a
+// time, so the partial outputs' loads are independent and many are in
+// flight at once: a serial walk over the splits is one L2 round trip per
+// split.
 template <int D>
 __global__ void __launch_bounds__(D) splitkv_merge_kernel(const float* o_part, const float* lse_part,
                                                          __nv_bfloat16* o, float* lse, int Nq,
                                                          int num_splits, const int* seq_lens,
                                                          int num_heads, long long split_keys,
                                                          int max_keys) {
+  static_assert(D % 32 == 0, "whole warps");
+  __shared__ float red[D / 32];
+  __shared__ float w_s[D];
   const int qi = blockIdx.x, bh = blockIdx.y, c = threadIdx.x;
+  const int lane = c & 31, warp = c >> 5;
   const size_t base = static_cast<size_t>(bh) * num_splits;
   // paged caches: an entry has only the splits that hold some of its keys
   // (the partial pass may skip the others and leave their slots unwritten)
@@ -37,15 +45,33 @@ __global__ void __launch_bounds__(D) splitkv_merge_kernel(const float* o_part, c
     const long long nk = max(0, min(seq_lens[bh / num_heads], max_keys));
     ns = static_cast<int>(min(static_cast<long long>(num_splits), (nk + split_keys - 1) / split_keys));
   }
-  float lmax = -INFINITY;
-  for (int s = 0; s < ns; ++s) lmax = fmaxf(lmax, lse_part[(base + s) * Nq + qi]);
+  auto lse_of = [&](int s) { return lse_part[(base + s) * Nq + qi]; };
+  // the largest split LSE
+  float m = -INFINITY;
+  for (int s = c; s < ns; s += D) m = fmaxf(m, lse_of(s));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  float lmax = red[0];
+#pragma unroll
+  for (int w = 1; w < D / 32; ++w) lmax = fmaxf(lmax, red[w]);
   float out = 0.f, lse_row = -INFINITY;
-  if (lmax != -INFINITY) {
+  if (lmax != -INFINITY) {  // uniform across the block
     float wsum = 0.f, acc = 0.f;
-    for (int s = 0; s < ns; ++s) {
-      const float w = __expf(lse_part[(base + s) * Nq + qi] - lmax);
-      wsum += w;
-      acc = fmaf(w, o_part[((base + s) * Nq + qi) * D + c], acc);
+    for (int s0 = 0; s0 < ns; s0 += D) {
+      const int n = min(D, ns - s0);
+      __syncthreads();  // the previous chunk's weights are no longer read
+      if (c < n) w_s[c] = __expf(lse_of(s0 + c) - lmax);
+      __syncthreads();
+      const float* src = o_part + ((base + s0) * Nq + qi) * D + c;
+      const size_t stride = static_cast<size_t>(Nq) * D;
+#pragma unroll 8
+      for (int i = 0; i < n; ++i) {
+        const float w = w_s[i];
+        wsum += w;
+        acc = fmaf(w, src[i * stride], acc);
+      }
     }
     out = acc / wsum;
     lse_row = lmax + __logf(wsum);

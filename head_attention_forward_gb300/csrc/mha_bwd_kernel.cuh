@@ -22,10 +22,15 @@
 // Both kernels share the forward kernel's shape: warp 0 feeds tiles with TMA
 // through mbarrier-guarded shared-memory slots, warp 1 allocates TMEM and
 // runs the tcgen05.mma issue loop (whole warp, one elected lane issues),
-// warps 4-7 own one TMEM lane (one row of the tile) per thread and do the
-// elementwise work; warps 2-3 only keep warps 4-7 on TMEM lane quarters.
-// P^T is written back to TMEM as bf16 over S^T, and dS (dS^T) over dP
-// (dP^T); each is the A operand of a later MMA straight from TMEM.
+// and warps 4-11 do the elementwise work, two threads per row of the tile
+// (one TMEM lane): warps 4-7 take columns 0-63 and warps 8-11 columns
+// 64-127.  The recomputed P needs no row-wise reduction (it comes from the
+// saved LSE), so the two halves never exchange anything.  Warps 2-3 only
+// keep warps 4-11 on TMEM lane quarters.  P^T is written back to TMEM as
+// bf16 over S^T, and dS (dS^T) over dP (dP^T), each packed into columns
+// 32-95 of its 128: every warp then overwrites only score columns it has
+// already read itself.  Each is the A operand of a later MMA straight from
+// TMEM.
 //
 // Every mbarrier wait is bounded (see mha_wait.cuh); a wait that runs out
 // records a status bit, raises the CTA's abort flag, and the CTA drains its
@@ -66,7 +71,7 @@ struct BwdCfg {
   // fixed pair (K,V for dK/dV; Q,dO for dQ), then the ring of pairs
   static constexpr int kOffFixed = 0;
   static constexpr int kOffRing = 2 * kTileBytes;
-  static constexpr int kOffRowBuf = kOffRing + kRing * 2 * kTileBytes;  // float [4 warps][2][128]
+  static constexpr int kOffRowBuf = kOffRing + kRing * 2 * kTileBytes;  // float [8 warps][2][64]
   static constexpr int kOffBar = kOffRowBuf + 4 * 128 * 8;
   // barriers: fixed_full ring_full[R] ring_empty[R] s_full dp_full p_ready
   //           ds_ready acc_full drain
@@ -81,10 +86,11 @@ struct BwdCfg {
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
   static_assert(kOffBar % 8 == 0 && kOffRing % 1024 == 0, "mbarrier / swizzle-atom alignment");
-  static constexpr int kThreads = 256;
+  static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
-  // scores [0,128), second product [128,256), accumulators from 256
-  static constexpr uint32_t kColS = 0, kColP2 = 128, kColAcc = 256;
+  // scores [0,128), second product [128,256), accumulators from 256; the
+  // bf16 P^T and dS are packed into columns 32-95 of the first two
+  static constexpr uint32_t kColS = 0, kColP2 = 128, kColAcc = 256, kPackOff = 32;
 };
 
 // D_i = sum_c dO_ic O_ic in fp32: one warp per row, rows [BH * N).
@@ -182,8 +188,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     }
     ptx::mbar_init(s_full, 1);
     ptx::mbar_init(dp_full, 1);
-    ptx::mbar_init(p_ready, 4);  // one elected arrive per elementwise warp
-    ptx::mbar_init(ds_ready, 4);
+    ptx::mbar_init(p_ready, 8);  // one elected arrive per elementwise warp
+    ptx::mbar_init(ds_ready, 8);
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -313,7 +319,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const bool more = t + 1 < n_steps;
       if (!(ok = wait_warp(p_ready, t & 1, ctl, kSiteMmaP))) break;
       ptx::tc_fence_after();
-      if constexpr (DKDV) issue_acc(tAcc0, tS, sRing(slot, 1), t == 0);  // dV += P^T dO_t
+      if constexpr (DKDV) issue_acc(tAcc0, tS + C::kPackOff, sRing(slot, 1), t == 0);  // dV += P^T dO_t
       if (more) {
         if (!(ok = ring_wait(t + 1))) break;
         ptx::tc_fence_after();
@@ -323,9 +329,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       if (!(ok = wait_warp(ds_ready, t & 1, ctl, kSiteMmaP))) break;
       ptx::tc_fence_after();
       if constexpr (DKDV)
-        issue_acc(tAcc1, tP2, sRing(slot, 0), t == 0);  // dK += dS^T Q_t
+        issue_acc(tAcc1, tP2 + C::kPackOff, sRing(slot, 0), t == 0);  // dK += dS^T Q_t
       else
-        issue_acc(tAcc0, tP2, sRing(slot, 0), t == 0);  // dQ += dS K_t
+        issue_acc(tAcc0, tP2 + C::kPackOff, sRing(slot, 0), t == 0);  // dQ += dS K_t
       commit(ring_empty(slot));
       if (more) {
         issue_scores(tP2, sFixed(1), sRing(nslot, 1));
@@ -339,18 +345,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------ elementwise rows
-    const int wq = warp & 3;  // TMEM lane quarter this warp may access
+    const int wq = warp & 3;            // TMEM lane quarter this warp may access
+    const int half = (warp - 4) >> 2;   // columns [64 * half, 64 * half + 64)
+    const int cbase = 64 * half;
     const int row = wq * 32 + lane;
     const int my = r0 + row;  // this thread's key (dK/dV) or query (dQ)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::kColS, tP2 = tmem + lane_off + C::kColP2;
+    const uint32_t tS = tmem + lane_off + C::kColS + cbase;      // this warp's score columns
+    const uint32_t tP2 = tmem + lane_off + C::kColP2 + cbase;    // and second-product columns
+    // where its 64 bf16 results go: 32 packed columns inside the 64 it reads
+    const uint32_t tSPack = tmem + lane_off + C::kColS + C::kPackOff + 32 * half;
+    const uint32_t tP2Pack = tmem + lane_off + C::kColP2 + C::kPackOff + 32 * half;
     const float sl2 = p.scale_log2;
     constexpr float kLog2e = 1.4426950408889634f;
     const size_t base = static_cast<size_t>(bh) * N;
-    // per-warp copy of the current query tile's LSE * log2 e and D (dK/dV),
-    // as two float[128] arrays so one 16-byte load covers four columns
-    float* lse_buf = reinterpret_cast<float*>(smem + C::kOffRowBuf) + (warp - 4) * 256;
-    float* d_buf = lse_buf + 128;
+    // per-warp copy of its 64 columns' LSE * log2 e and D (dK/dV), as two
+    // float[64] arrays so one 16-byte load covers four columns
+    float* lse_buf = reinterpret_cast<float*>(smem + C::kOffRowBuf) + (warp - 4) * 128;
+    float* d_buf = lse_buf + 64;
     // this row's own (LSE * log2 e, D) (dQ); rows past N see no key
     float my_lse2 = INFINITY, my_d = 0.f;
     if (!DKDV && my < N) {
@@ -362,9 +374,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const int y0 = (t_begin + t) * C::kBlock;  // first column's query (dK/dV) or key (dQ)
       if constexpr (DKDV) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < 2; ++m) {
           const int c = lane + 32 * m;
-          const int qi = y0 + c;
+          const int qi = y0 + cbase + c;
           // a query past N has LSE = +inf here, so its P and dS are 0
           lse_buf[c] = qi < N ? p.lse[base + qi] * kLog2e : INFINITY;
           d_buf[c] = qi < N ? p.dsum[base + qi] : 0.f;
@@ -381,48 +393,48 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
-      // P over this row's 128 columns, kept in registers for dS; in four
-      // 32-column chunks, chunk k's bf16 values go to columns [16k, 16k+16),
-      // which earlier loads have already read
-      float pr[128];
+      // P over this thread's 64 columns, kept in registers for dS.  All 64
+      // scores are read before any P goes back over them.
+      float pr[64];
+      {
+        uint32_t sr[64];
+        ptx::tmem_ld_x64(tS, sr);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t sr[32];
-        ptx::tmem_ld_x32(tS + 32 * k, sr);
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const int c = 32 * k + 4 * i4;
+        for (int i4 = 0; i4 < 16; ++i4) {
+          const int c = 4 * i4;
           const float4 l4 = DKDV ? *reinterpret_cast<const float4*>(lse_buf + c)
                                  : make_float4(my_lse2, my_lse2, my_lse2, my_lse2);
-          pr[c] = ptx::ex2(__uint_as_float(sr[4 * i4]) * sl2 - l4.x);
-          pr[c + 1] = ptx::ex2(__uint_as_float(sr[4 * i4 + 1]) * sl2 - l4.y);
-          pr[c + 2] = ptx::ex2(__uint_as_float(sr[4 * i4 + 2]) * sl2 - l4.z);
-          pr[c + 3] = ptx::ex2(__uint_as_float(sr[4 * i4 + 3]) * sl2 - l4.w);
+          pr[c] = ptx::ex2(__uint_as_float(sr[c]) * sl2 - l4.x);
+          pr[c + 1] = ptx::ex2(__uint_as_float(sr[c + 1]) * sl2 - l4.y);
+          pr[c + 2] = ptx::ex2(__uint_as_float(sr[c + 2]) * sl2 - l4.z);
+          pr[c + 3] = ptx::ex2(__uint_as_float(sr[c + 3]) * sl2 - l4.w);
         }
-        if (edge) {
+      }
+      if (edge) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = 32 * k + i;
-            bool vis;
-            if constexpr (DKDV) {
-              vis = !CAUSAL || my <= y0 + c;  // key my, query y0 + c
-            } else {
-              const int key = y0 + c;
-              vis = key < N && (!CAUSAL || key <= my);
-            }
-            pr[c] = vis ? pr[c] : 0.f;
+        for (int c = 0; c < 64; ++c) {
+          bool vis;
+          if constexpr (DKDV) {
+            vis = !CAUSAL || my <= y0 + cbase + c;  // key my, query y0 + cbase + c
+          } else {
+            const int key = y0 + cbase + c;
+            vis = key < N && (!CAUSAL || key <= my);
           }
+          pr[c] = vis ? pr[c] : 0.f;
         }
-        if constexpr (DKDV) {
+      }
+      if constexpr (DKDV) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(pr[32 * k + 2 * i], pr[32 * k + 2 * i + 1]);
-          ptx::tmem_st_x16(tS + 16 * k, pk);  // P^T over S^T
+          ptx::tmem_st_x16(tSPack + 16 * k, pk);  // P^T over S^T
         }
+        ptx::tmem_wait_st();
       }
       // dK/dV: P^T is in TMEM; dQ: S has been read.  Either way the issuer
       // may go on (dV += P^T dO, or the next tile's scores over S).
-      if constexpr (DKDV) ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(p_ready);
@@ -431,23 +443,25 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         break;
       }
       ptx::tc_fence_after();
+      {
+        uint32_t dr[64];
+        ptx::tmem_ld_x64(tP2, dr);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        uint32_t dr[32];
-        ptx::tmem_ld_x32(tP2 + 32 * k, dr);
-        uint32_t pk[16];
+        for (int k = 0; k < 2; ++k) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const int c = 32 * k + 4 * i4;
-          const float4 d4 = DKDV ? *reinterpret_cast<const float4*>(d_buf + c)
-                                 : make_float4(my_d, my_d, my_d, my_d);
-          pk[2 * i4] = ptx::pack_bf16x2(pr[c] * (__uint_as_float(dr[4 * i4]) - d4.x),
-                                        pr[c + 1] * (__uint_as_float(dr[4 * i4 + 1]) - d4.y));
-          pk[2 * i4 + 1] = ptx::pack_bf16x2(pr[c + 2] * (__uint_as_float(dr[4 * i4 + 2]) - d4.z),
-                                            pr[c + 3] * (__uint_as_float(dr[4 * i4 + 3]) - d4.w));
+          for (int i4 = 0; i4 < 8; ++i4) {
+            const int c = 32 * k + 4 * i4;
+            const float4 d4 = DKDV ? *reinterpret_cast<const float4*>(d_buf + c)
+                                   : make_float4(my_d, my_d, my_d, my_d);
+            pk[2 * i4] = ptx::pack_bf16x2(pr[c] * (__uint_as_float(dr[c]) - d4.x),
+                                          pr[c + 1] * (__uint_as_float(dr[c + 1]) - d4.y));
+            pk[2 * i4 + 1] = ptx::pack_bf16x2(pr[c + 2] * (__uint_as_float(dr[c + 2]) - d4.z),
+                                              pr[c + 3] * (__uint_as_float(dr[c + 3]) - d4.w));
+          }
+          // dS^T over dP^T (dK/dV) or dS over dP (dQ)
+          ptx::tmem_st_x16(tP2Pack + 16 * k, pk);
         }
-        // dS^T over dP^T (dK/dV) or dS over dP (dQ)
-        ptx::tmem_st_x16(tP2 + 16 * k, pk);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -457,7 +471,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     if (ok && n_steps > 0 && wait_warp(acc_full, 0, ctl, kSiteSoftmaxO)) {
       ptx::tc_fence_after();
       const bool valid = my < N;
-      // epilogue: accumulators -> bf16 rows (dK and dQ carry the scale)
+      // epilogue: accumulators -> bf16 rows (dK and dQ carry the scale);
+      // each half of the warps writes half of every row
 #pragma unroll 1
       for (int which = 0; which < (DKDV ? 2 : 1); ++which) {
         __nv_bfloat16* out = DKDV ? (which == 0 ? p.dv : p.dk) : p.dq;
@@ -465,7 +480,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
         const uint32_t tacc = tmem + lane_off + C::kColAcc + which * D;
         __nv_bfloat16* orow = out + (base + (valid ? my : 0)) * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {
           uint32_t av[32];
           ptx::tmem_ld_x32(tacc + c * 32, av);
           uint32_t pk[16];

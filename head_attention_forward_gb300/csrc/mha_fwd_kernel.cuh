@@ -40,6 +40,15 @@
 // The tensor pipe executes one thread's MMAs in issue order, so issuing
 // S_{j+1}(s) after PV_j(s) cannot clobber P_j(s) before it is read.
 //
+// Split mode (SPLIT) serves split-KV decoding, a few queries against a long
+// key sequence: work tiles are (head, key split) pairs that warp 0 hands out
+// at run time; the queries (at most 32) sit in the first softmax warp of
+// stage 0 and the other softmax warps have no work; the scores are
+// double-buffered in both stages' S columns, so S_{j+1} is computed while
+// the softmax works on S_j; each split writes an fp32 partial output and
+// its LSE for a merge kernel.  PAGED gathers each 128-key tile of a paged
+// K/V cache from page-sized TMA boxes named by a block table.
+//
 // Every mbarrier wait is bounded (clock64 budget).  A wait that runs out
 // records a code in the device status word, raises a CTA-wide abort flag
 // that ends every other wait at once, and the CTA then drains its own
@@ -62,8 +71,8 @@ struct FwdParams {
   int N;
   int num_mblocks;     // ceil(N / 256)
   int BH;              // batch * heads; work tiles are (bh, m-block) pairs
-  // split mode only: Nq queries per head (one Q tile, rows past Nq read as
-  // zeros) against Nk keys cut into num_splits runs of tiles_per_split
+  // split mode only: Nq <= 32 queries per head (one Q tile, rows past Nq
+  // read as zeros) against Nk keys cut into num_splits runs of tiles_per_split
   // K/V tiles; work tiles are (bh, split) pairs and each writes an fp32
   // partial output normalised by its own sum, plus its log-sum-exp
   int Nq, Nk, num_splits, tiles_per_split;

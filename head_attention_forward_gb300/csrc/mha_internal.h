@@ -26,7 +26,7 @@ bool encode_paged_map(CUtensorMap* map, const void* base, int num_blocks, int H,
                       int box_rows);
 
 // The partial pass of split-KV decoding on the tensor cores (the persistent
-// attention kernel in split mode): Nq <= 128 queries per head against Nk
+// attention kernel in split mode): Nq <= 32 queries per head against Nk
 // keys, num_splits runs of tiles_per_split 128-key tiles, fp32 partial
 // outputs for the merge kernel.  tile_counter is one int of device memory
 // the pass zeroes (on `st`) and then uses to hand out work tiles.

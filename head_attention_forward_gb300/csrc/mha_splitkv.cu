@@ -50,6 +50,9 @@ Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits) {
   return pl;
 }
 
+// the split pass keeps every query row in the first softmax warp
+static_assert(mha::kSplitMaxQ <= 32, "query rows per split-pass work tile");
+
 int check_shape(int B, int H, int Nq, int Nk, int d, int num_splits) {
   if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || num_splits < 0) return MHA_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return MHA_ERR_UNSUPPORTED_DIM;

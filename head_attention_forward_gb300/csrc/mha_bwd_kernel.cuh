@@ -68,18 +68,24 @@ struct BwdCfg {
   static constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 bytes
   static constexpr int kTileBytes = kHalves * kHalfBytes;
   static constexpr int kRing = (D == 128) ? 2 : 3;  // slots of two tiles each
+  // the dQ kernel splits the same space into a K ring and a V ring: V_j is
+  // free as soon as dP_j is done, K_j only after dQ += dS K_j
+  static constexpr int kKRing = (D == 128) ? 3 : 4, kVRing = 2 * kRing - kKRing;
   // fixed pair (K,V for dK/dV; Q,dO for dQ), then the ring of pairs
   static constexpr int kOffFixed = 0;
   static constexpr int kOffRing = 2 * kTileBytes;
   static constexpr int kOffRowBuf = kOffRing + kRing * 2 * kTileBytes;  // float [8 warps][2][64]
   static constexpr int kOffBar = kOffRowBuf + 4 * 128 * 8;
-  // barriers: fixed_full ring_full[R] ring_empty[R] s_full dp_full p_ready
-  //           ds_ready acc_full drain
-  static constexpr int kBarFixed = 0, kBarRingFull = 1, kBarRingEmpty = 1 + kRing;
-  static constexpr int kBarSFull = 1 + 2 * kRing, kBarDpFull = kBarSFull + 1;
+  // barriers: fixed_full ring_full[2R] ring_empty[2R] s_full dp_full[2]
+  //           p_ready ds_ready[2] acc_full drain
+  // dK/dV uses ring_*[0, R) (one per pair slot), dp_full[0] and ds_ready[0];
+  // dQ uses ring_*[0, kKRing) for K, ring_*[kKRing, 2R) for V, and one
+  // dp_full / ds_ready per second-product buffer
+  static constexpr int kBarFixed = 0, kBarRingFull = 1, kBarRingEmpty = 1 + 2 * kRing;
+  static constexpr int kBarSFull = 1 + 4 * kRing, kBarDpFull = kBarSFull + 1;
   // p_ready: P^T written back (dK/dV), or S read into registers (dQ)
-  static constexpr int kBarPReady = kBarDpFull + 1, kBarDsReady = kBarPReady + 1;
-  static constexpr int kBarAcc = kBarDsReady + 1, kBarDrain = kBarAcc + 1;
+  static constexpr int kBarPReady = kBarDpFull + 2, kBarDsReady = kBarPReady + 1;
+  static constexpr int kBarAcc = kBarDsReady + 2, kBarDrain = kBarAcc + 1;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
@@ -89,8 +95,11 @@ struct BwdCfg {
   static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
   // scores [0,128), second product [128,256), accumulators from 256; the
-  // bf16 P^T and dS are packed into columns 32-95 of the first two
+  // bf16 P^T and dS are packed into columns 32-95 of the first two.  The dQ
+  // kernel has one accumulator, so it double-buffers the second product
+  // ([128,256) and [256,384)) and keeps dQ at [384, 384 + D).
   static constexpr uint32_t kColS = 0, kColP2 = 128, kColAcc = 256, kPackOff = 32;
+  static constexpr uint32_t kColP2b = 256, kColAccQ = 384;
 };
 
 // D_i = sum_c dO_ic O_ic in fp32: one warp per row, rows [BH * N).
@@ -164,10 +173,24 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   auto ring_full = [&](int i) { return bar(C::kBarRingFull + i); };
   auto ring_empty = [&](int i) { return bar(C::kBarRingEmpty + i); };
   const uint32_t s_full = bar(C::kBarSFull);    // scores in TMEM
-  const uint32_t dp_full = bar(C::kBarDpFull);  // dO.V products in TMEM
+  // dO.V products in TMEM, per buffer (dK/dV: one buffer; dQ: step t uses t & 1)
+  auto dp_full = [&](int b) { return bar(C::kBarDpFull + b); };
   // dK/dV: P^T written back over S^T; dQ: S read into registers
   const uint32_t p_ready = bar(C::kBarPReady);
-  const uint32_t ds_ready = bar(C::kBarDsReady);  // dS (dS^T) written back over dP (dP^T)
+  // dS (dS^T) written back over dP (dP^T), per buffer like dp_full
+  auto ds_ready = [&](int b) { return bar(C::kBarDsReady + b); };
+  // the buffer and the phase parity of step t's second product
+  auto p2_buf = [](int t) { return DKDV ? 0 : (t & 1); };
+  auto p2_par = [](int t) { return static_cast<uint32_t>(DKDV ? (t & 1) : ((t >> 1) & 1)); };
+  auto p2_col = [&](int t) -> uint32_t { return p2_buf(t) ? C::kColP2b : C::kColP2; };
+  constexpr uint32_t kColAccK = DKDV ? C::kColAcc : C::kColAccQ;
+  // dQ: K_j in K slot j % kKRing, V_j in V slot j % kVRing
+  auto sK = [&](int i) -> uint32_t { return sbase + C::kOffRing + i * C::kTileBytes; };
+  auto sV = [&](int i) -> uint32_t { return sbase + C::kOffRing + (C::kKRing + i) * C::kTileBytes; };
+  auto k_full = [&](int t) { return ring_full(t % C::kKRing); };
+  auto k_empty = [&](int t) { return ring_empty(t % C::kKRing); };
+  auto v_full = [&](int t) { return ring_full(C::kKRing + t % C::kVRing); };
+  auto v_empty = [&](int t) { return ring_empty(C::kKRing + t % C::kVRing); };
   const uint32_t acc_full = bar(C::kBarAcc);
   const uint32_t drain_bar = bar(C::kBarDrain);
   // fixed pair: [0] K or Q, [1] V or dO; ring slot i: [0] Q or K, [1] dO or V
@@ -182,14 +205,16 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(fixed_full, 1);
-    for (int i = 0; i < C::kRing; ++i) {
+    for (int i = 0; i < 2 * C::kRing; ++i) {
       ptx::mbar_init(ring_full(i), 1);
       ptx::mbar_init(ring_empty(i), 1);
     }
     ptx::mbar_init(s_full, 1);
-    ptx::mbar_init(dp_full, 1);
     ptx::mbar_init(p_ready, 8);  // one elected arrive per elementwise warp
-    ptx::mbar_init(ds_ready, 8);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(dp_full(b), 1);
+      ptx::mbar_init(ds_ready(b), 8);
+    }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -215,42 +240,54 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   const CUtensorMap* ring0 = DKDV ? &tmQ : &tmK;
   const CUtensorMap* ring1 = DKDV ? &tmDO : &tmV;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
+  if (warp == 0 || (!DKDV && warp == 3)) {
+    // ----------------------------------------------------------- producers
+    // Warp 0 loads the fixed pair, then (dK/dV) the ring of (Q_i, dO_i)
+    // pairs or (dQ) the K ring; in the dQ kernel warp 3 loads the V ring,
+    // each at its own pace.
     if (lane == 0 && n_steps > 0) {
-      ptx::mbar_arrive_expect_tx(fixed_full, 2 * C::kTileBytes);
-      for (int h = 0; h < C::kHalves; ++h) {
-        ptx::tma_load_3d(sFixed(0) + h * C::kHalfBytes, fixed0, fixed_full, h * 64, r0, bh);
-        ptx::tma_load_3d(sFixed(1) + h * C::kHalfBytes, fixed1, fixed_full, h * 64, r0, bh);
+      if (warp == 0) {
+        ptx::mbar_arrive_expect_tx(fixed_full, 2 * C::kTileBytes);
+        for (int h = 0; h < C::kHalves; ++h) {
+          ptx::tma_load_3d(sFixed(0) + h * C::kHalfBytes, fixed0, fixed_full, h * 64, r0, bh);
+          ptx::tma_load_3d(sFixed(1) + h * C::kHalfBytes, fixed1, fixed_full, h * 64, r0, bh);
+        }
       }
+      // one ring: pairs (dK/dV), K tiles or V tiles (dQ)
+      const bool is_v = !DKDV && warp == 3;
+      const int depth = DKDV ? C::kRing : (is_v ? C::kVRing : C::kKRing);
+      const int per_slot = DKDV ? 2 : 1;  // tiles per slot
+      auto full_of = [&](int t) { return DKDV ? ring_full(t % C::kRing) : (is_v ? v_full(t) : k_full(t)); };
+      auto empty_of = [&](int t) { return DKDV ? ring_empty(t % C::kRing) : (is_v ? v_empty(t) : k_empty(t)); };
+      auto dst_of = [&](int t, int w) -> uint32_t {
+        return DKDV ? sRing(t % C::kRing, w) : (is_v ? sV(t % C::kVRing) : sK(t % C::kKRing));
+      };
+      auto map_of = [&](int w) -> const CUtensorMap* { return DKDV ? (w ? ring1 : ring0) : (is_v ? &tmV : &tmK); };
       int t = 0;
       bool ok = true;
       for (; t < n_steps; ++t) {
-        const int slot = t % C::kRing;
-        const int use = t / C::kRing;
-        if (use > 0 && !wait_one(ring_empty(slot), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
+        const int use = t / depth;
+        if (use > 0 && !wait_one(empty_of(t), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
           ok = false;
           break;
         }
         const int y = (t_begin + t) * C::kBlock;
-        ptx::mbar_arrive_expect_tx(ring_full(slot), 2 * C::kTileBytes);
-        for (int h = 0; h < C::kHalves; ++h) {
-          ptx::tma_load_3d(sRing(slot, 0) + h * C::kHalfBytes, ring0, ring_full(slot), h * 64, y, bh);
-          ptx::tma_load_3d(sRing(slot, 1) + h * C::kHalfBytes, ring1, ring_full(slot), h * 64, y, bh);
-        }
-        if (t + 2 < n_steps) {  // warm L2 two steps ahead (the ring holds two)
-          const int y2 = (t_begin + t + 2) * C::kBlock;
-          for (int h = 0; h < C::kHalves; ++h) {
-            ptx::tma_prefetch_3d(ring0, h * 64, y2, bh);
-            ptx::tma_prefetch_3d(ring1, h * 64, y2, bh);
-          }
+        ptx::mbar_arrive_expect_tx(full_of(t), per_slot * C::kTileBytes);
+        for (int w = 0; w < per_slot; ++w)
+          for (int h = 0; h < C::kHalves; ++h)
+            ptx::tma_load_3d(dst_of(t, w) + h * C::kHalfBytes, map_of(w), full_of(t), h * 64, y, bh);
+        // warm L2 one ring's depth ahead (two steps for the one-slot V ring)
+        const int ahead = t + max(depth, 2);
+        if (ahead < n_steps) {
+          const int y2 = (t_begin + ahead) * C::kBlock;
+          for (int w = 0; w < per_slot; ++w)
+            for (int h = 0; h < C::kHalves; ++h) ptx::tma_prefetch_3d(map_of(w), h * 64, y2, bh);
         }
       }
       if (!ok) {
         // let the copies already issued land before the CTA goes away
-        drain_wait(fixed_full, 0, ctl);
-        for (int u = max(0, t - C::kRing); u < t; ++u)
-          drain_wait(ring_full(u % C::kRing), (u / C::kRing) & 1, ctl);
+        if (warp == 0) drain_wait(fixed_full, 0, ctl);
+        for (int u = max(0, t - depth); u < t; ++u) drain_wait(full_of(u), (u / depth) & 1, ctl);
       }
     }
     __syncwarp();
@@ -259,8 +296,8 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // Every lane runs the loop with the same values; an elected lane issues.
     constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t kIdescAcc = ptx::idesc_bf16_f32(128, D, 0, 1);
-    const uint32_t tS = tmem + C::kColS, tP2 = tmem + C::kColP2;
-    const uint32_t tAcc0 = tmem + C::kColAcc, tAcc1 = tmem + C::kColAcc + D;
+    const uint32_t tS = tmem + C::kColS;
+    const uint32_t tAcc0 = tmem + kColAccK, tAcc1 = tmem + kColAccK + D;
     // K-major views (rows x d, 128-byte swizzle, 8-row groups 1 KiB apart)
     // and MN-major views (d contiguous, d-halves 16 KiB apart) of a tile
     auto kmaj = [](uint32_t a) { return ptx::desc_sw128(a, 16, 1024); };
@@ -295,23 +332,41 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     };
     bool ok = n_steps > 0 && wait_warp(fixed_full, 0, ctl, kSiteMmaQ);
     // The scores of the next tile are computed while this tile's dS is being
-    // made, and the next dO.V product while its P is: per tile the tensor
-    // core sees
+    // made, and (dK/dV) the next dO.V product while its P is: per tile the
+    // tensor core sees
     //   dK/dV: dV += P^T dO_t | S^T_{t+1} | dK += dS^T Q_t | dP^T_{t+1}
-    //   dQ:    S_{t+1} | dQ += dS K_t | dP_{t+1}
-    // Each product overwrites TMEM that an earlier one in this order reads
-    // (P^T over S^T, dS over dP), which the tensor pipe's in-order execution
-    // makes safe; the elementwise side has read those columns before it
-    // signals.
+    //   dQ:    S_{t+1} | dP_{t+1} | dQ += dS K_t
+    // dQ double-buffers dP, so dP_{t+1} need not wait for dS_t: the
+    // elementwise warps make dS_{t+1} while the tensor core still works on
+    // dQ_t.  Each product overwrites TMEM that an earlier one in this order
+    // reads (P^T over S^T, dS over dP, dP_{t+1} over dS_{t-1}), which the
+    // tensor pipe's in-order execution makes safe; the elementwise side has
+    // read those columns before it signals.  No barrier can complete two
+    // phases ahead of its waiter: each next-but-one phase needs an action
+    // that follows the waiter's observation of the current one.
     auto ring_wait = [&](int t) {
       return wait_warp(ring_full(t % C::kRing), (t / C::kRing) & 1, ctl, kSiteMmaKV);
     };
-    if (ok && (ok = ring_wait(0))) {
-      ptx::tc_fence_after();
-      issue_scores(tS, sFixed(0), sRing(0, 0));   // S^T = K Q_0^T  |  S = Q K_0^T
-      commit(s_full);
-      issue_scores(tP2, sFixed(1), sRing(0, 1));  // dP^T = V dO_0^T  |  dP = dO V_0^T
-      commit(dp_full);
+    if constexpr (DKDV) {
+      if (ok && (ok = ring_wait(0))) {
+        ptx::tc_fence_after();
+        issue_scores(tS, sFixed(0), sRing(0, 0));                // S^T = K Q_0^T
+        commit(s_full);
+        issue_scores(tmem + C::kColP2, sFixed(1), sRing(0, 1));  // dP^T = V dO_0^T
+        commit(dp_full(0));
+      }
+    } else {
+      if (ok && (ok = wait_warp(k_full(0), 0, ctl, kSiteMmaKV))) {
+        ptx::tc_fence_after();
+        issue_scores(tS, sFixed(0), sK(0));  // S = Q K_0^T
+        commit(s_full);
+      }
+      if (ok && (ok = wait_warp(v_full(0), 0, ctl, kSiteMmaKV))) {
+        ptx::tc_fence_after();
+        issue_scores(tmem + p2_col(0), sFixed(1), sV(0));  // dP = dO V_0^T
+        commit(dp_full(0));
+        commit(v_empty(0));
+      }
     }
     for (int t = 0; t < n_steps && ok; ++t) {
       const int slot = t % C::kRing;
@@ -319,23 +374,39 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       const bool more = t + 1 < n_steps;
       if (!(ok = wait_warp(p_ready, t & 1, ctl, kSiteMmaP))) break;
       ptx::tc_fence_after();
-      if constexpr (DKDV) issue_acc(tAcc0, tS + C::kPackOff, sRing(slot, 1), t == 0);  // dV += P^T dO_t
+      if constexpr (!DKDV) {
+        if (more) {
+          const int u = t + 1;
+          if (!(ok = wait_warp(k_full(u), (u / C::kKRing) & 1, ctl, kSiteMmaKV))) break;
+          ptx::tc_fence_after();
+          issue_scores(tS, sFixed(0), sK(u % C::kKRing));  // S_{t+1}
+          commit(s_full);
+          if (!(ok = wait_warp(v_full(u), (u / C::kVRing) & 1, ctl, kSiteMmaKV))) break;
+          ptx::tc_fence_after();
+          issue_scores(tmem + p2_col(u), sFixed(1), sV(u % C::kVRing));  // dP_{t+1}
+          commit(dp_full(p2_buf(u)));
+          commit(v_empty(u));
+        }
+        if (!(ok = wait_warp(ds_ready(p2_buf(t)), p2_par(t), ctl, kSiteMmaP))) break;
+        ptx::tc_fence_after();
+        issue_acc(tAcc0, tmem + p2_col(t) + C::kPackOff, sK(t % C::kKRing), t == 0);  // dQ += dS K_t
+        commit(k_empty(t));
+        continue;
+      }
+      issue_acc(tAcc0, tS + C::kPackOff, sRing(slot, 1), t == 0);  // dV += P^T dO_t
       if (more) {
         if (!(ok = ring_wait(t + 1))) break;
         ptx::tc_fence_after();
         issue_scores(tS, sFixed(0), sRing(nslot, 0));
         commit(s_full);
       }
-      if (!(ok = wait_warp(ds_ready, t & 1, ctl, kSiteMmaP))) break;
+      if (!(ok = wait_warp(ds_ready(0), t & 1, ctl, kSiteMmaP))) break;
       ptx::tc_fence_after();
-      if constexpr (DKDV)
-        issue_acc(tAcc1, tP2 + C::kPackOff, sRing(slot, 0), t == 0);  // dK += dS^T Q_t
-      else
-        issue_acc(tAcc0, tP2 + C::kPackOff, sRing(slot, 0), t == 0);  // dQ += dS K_t
+      issue_acc(tAcc1, tmem + C::kColP2 + C::kPackOff, sRing(slot, 0), t == 0);  // dK += dS^T Q_t
       commit(ring_empty(slot));
       if (more) {
-        issue_scores(tP2, sFixed(1), sRing(nslot, 1));
-        commit(dp_full);
+        issue_scores(tmem + C::kColP2, sFixed(1), sRing(nslot, 1));  // dP^T_{t+1}
+        commit(dp_full(0));
       }
     }
     if (ok) commit(acc_full);
@@ -351,11 +422,9 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     const int row = wq * 32 + lane;
     const int my = r0 + row;  // this thread's key (dK/dV) or query (dQ)
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tS = tmem + lane_off + C::kColS + cbase;      // this warp's score columns
-    const uint32_t tP2 = tmem + lane_off + C::kColP2 + cbase;    // and second-product columns
+    const uint32_t tS = tmem + lane_off + C::kColS + cbase;  // this warp's score columns
     // where its 64 bf16 results go: 32 packed columns inside the 64 it reads
     const uint32_t tSPack = tmem + lane_off + C::kColS + C::kPackOff + 32 * half;
-    const uint32_t tP2Pack = tmem + lane_off + C::kColP2 + C::kPackOff + 32 * half;
     const float sl2 = p.scale_log2;
     constexpr float kLog2e = 1.4426950408889634f;
     const size_t base = static_cast<size_t>(bh) * N;
@@ -438,11 +507,14 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(p_ready);
-      if (!wait_warp(dp_full, t & 1, ctl, kSiteSoftmaxS)) {
+      if (!wait_warp(dp_full(p2_buf(t)), p2_par(t), ctl, kSiteSoftmaxS)) {
         ok = false;
         break;
       }
       ptx::tc_fence_after();
+      // this step's second-product columns, and the packed dS over them
+      const uint32_t tP2 = tmem + lane_off + p2_col(t) + cbase;
+      const uint32_t tP2Pack = tmem + lane_off + p2_col(t) + C::kPackOff + 32 * half;
       {
         uint32_t dr[64];
         ptx::tmem_ld_x64(tP2, dr);
@@ -466,7 +538,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(ds_ready);
+      if (lane == 0) ptx::mbar_arrive(ds_ready(p2_buf(t)));
     }
     if (ok && n_steps > 0 && wait_warp(acc_full, 0, ctl, kSiteSoftmaxO)) {
       ptx::tc_fence_after();
@@ -477,7 +549,7 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
       for (int which = 0; which < (DKDV ? 2 : 1); ++which) {
         __nv_bfloat16* out = DKDV ? (which == 0 ? p.dv : p.dk) : p.dq;
         const float mul = (DKDV && which == 0) ? 1.f : p.scale;
-        const uint32_t tacc = tmem + lane_off + C::kColAcc + which * D;
+        const uint32_t tacc = tmem + lane_off + kColAccK + which * D;
         __nv_bfloat16* orow = out + (base + (valid ? my : 0)) * D;
 #pragma unroll
         for (int c = half * (D / 64); c < (half + 1) * (D / 64); ++c) {

@@ -63,7 +63,8 @@ cudaError_t launch_all(const CUtensorMap& mq, const CUtensorMap& mk, const CUten
                        const void* dout, float* dsum, long long BH, int N, bool causal,
                        cudaStream_t st) {
   const long long rows = BH * N;
-  mha::bwd_rowdot_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(
+  constexpr int kRows = mha::RowdotCfg<D>::kRowsPerBlock;
+  mha::bwd_rowdot_kernel<D><<<static_cast<unsigned>((rows + kRows - 1) / kRows), 256, 0, st>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), dsum, rows);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;

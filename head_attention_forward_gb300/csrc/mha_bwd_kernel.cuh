@@ -102,37 +102,40 @@ struct BwdCfg {
   static constexpr uint32_t kColP2b = 256, kColAccQ = 384;
 };
 
-// D_i = sum_c dO_ic O_ic in fp32: one warp per row, rows [BH * N).
+// D_i = sum_c dO_ic O_ic in fp32 over rows [0, rows).  A thread reads 16
+// bytes (8 elements) of each, so D/8 lanes cover a row and a 256-thread
+// block covers kRowsPerBlock rows.
+template <int D>
+struct RowdotCfg {
+  static constexpr int kLanesPerRow = D / 8;
+  static constexpr int kRowsPerBlock = 256 / kLanesPerRow;
+};
+
 template <int D>
 __global__ void __launch_bounds__(256) bwd_rowdot_kernel(const __nv_bfloat16* __restrict__ o,
                                                          const __nv_bfloat16* __restrict__ dout,
                                                          float* __restrict__ dsum,
                                                          long long rows) {
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  constexpr int kPer = D / 32;  // elements per lane: 2 or 4
-  const __nv_bfloat16* a = o + row * D + lane * kPer;
-  const __nv_bfloat16* b = dout + row * D + lane * kPer;
+  constexpr int kL = RowdotCfg<D>::kLanesPerRow;
+  const long long row = static_cast<long long>(blockIdx.x) * RowdotCfg<D>::kRowsPerBlock + threadIdx.x / kL;
+  const int sub = threadIdx.x % kL;
   float acc = 0.f;
-  if constexpr (kPer == 4) {
-    const uint2 ua = *reinterpret_cast<const uint2*>(a);
-    const uint2 ub = *reinterpret_cast<const uint2*>(b);
-    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ua.x));
-    const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ua.y));
-    const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ub.x));
-    const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ub.y));
-    acc = a0.x * b0.x + a0.y * b0.y + a1.x * b1.x + a1.y * b1.y;
-  } else {
-    const uint32_t ua = *reinterpret_cast<const uint32_t*>(a);
-    const uint32_t ub = *reinterpret_cast<const uint32_t*>(b);
-    const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ua));
-    const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ub));
-    acc = a0.x * b0.x + a0.y * b0.y;
-  }
+  if (row < rows) {
+    const uint4 ua = *reinterpret_cast<const uint4*>(o + row * D + sub * 8);
+    const uint4 ub = *reinterpret_cast<const uint4*>(dout + row * D + sub * 8);
+    const uint32_t wa[4] = {ua.x, ua.y, ua.z, ua.w}, wb[4] = {ub.x, ub.y, ub.z, ub.w};
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dsum[row] = acc;
+    for (int e = 0; e < 4; ++e) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wa[e]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wb[e]));
+      acc = fmaf(a.x, b.x, acc);
+      acc = fmaf(a.y, b.y, acc);
+    }
+  }
+  // every lane takes part in the shuffles (rows past the end add zeros)
+#pragma unroll
+  for (int off = kL / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && sub == 0) dsum[row] = acc;
 }
 
 // Shared skeleton of the two tile kernels.  DKDV = true: one CTA per

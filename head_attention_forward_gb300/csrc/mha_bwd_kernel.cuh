@@ -67,20 +67,22 @@ struct BwdCfg {
   static constexpr int kHalves = D / 64;         // 128-byte swizzle atoms across d
   static constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 bytes
   static constexpr int kTileBytes = kHalves * kHalfBytes;
-  static constexpr int kRing = (D == 128) ? 2 : 3;  // slots of two tiles each
-  // the dQ kernel splits the same space into a K ring and a V ring: V_j is
-  // free as soon as dP_j is done, K_j only after dQ += dS K_j
-  static constexpr int kKRing = (D == 128) ? 3 : 4, kVRing = 2 * kRing - kKRing;
-  // fixed pair (K,V for dK/dV; Q,dO for dQ), then the ring of pairs
+  static constexpr int kRing = (D == 128) ? 2 : 3;  // the rings' space, in tile pairs
+  // The other side's tiles come through two rings: ring A carries the
+  // score product's operand (Q_i for dK/dV, K_j for dQ), ring B the second
+  // product's (dO_i, V_j).  B's tile is free once the products that read
+  // it are done (dP^T and dV += P^T dO; dP), A's only after the last one
+  // (dK += dS^T Q; dQ += dS K), so A gets the deeper ring.
+  static constexpr int kARing = (D == 128) ? 3 : 4, kBRing = 2 * kRing - kARing;
+  // fixed pair (K,V for dK/dV; Q,dO for dQ), then ring A, then ring B
   static constexpr int kOffFixed = 0;
   static constexpr int kOffRing = 2 * kTileBytes;
   static constexpr int kOffRowBuf = kOffRing + kRing * 2 * kTileBytes;  // float [8 warps][2][64]
   static constexpr int kOffBar = kOffRowBuf + 4 * 128 * 8;
   // barriers: fixed_full ring_full[2R] ring_empty[2R] s_full dp_full[2]
   //           p_ready ds_ready[2] acc_full drain
-  // dK/dV uses ring_*[0, R) (one per pair slot), dp_full[0] and ds_ready[0];
-  // dQ uses ring_*[0, kKRing) for K, ring_*[kKRing, 2R) for V, and one
-  // dp_full / ds_ready per second-product buffer
+  // ring_*[0, kARing) serve ring A and ring_*[kARing, 2R) ring B; dK/dV
+  // uses dp_full[0] and ds_ready[0], dQ one of each per dP buffer
   static constexpr int kBarFixed = 0, kBarRingFull = 1, kBarRingEmpty = 1 + 2 * kRing;
   static constexpr int kBarSFull = 1 + 4 * kRing, kBarDpFull = kBarSFull + 1;
   // p_ready: P^T written back (dK/dV), or S read into registers (dQ)
@@ -187,20 +189,20 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
   auto p2_par = [](int t) { return static_cast<uint32_t>(DKDV ? (t & 1) : ((t >> 1) & 1)); };
   auto p2_col = [&](int t) -> uint32_t { return p2_buf(t) ? C::kColP2b : C::kColP2; };
   constexpr uint32_t kColAccK = DKDV ? C::kColAcc : C::kColAccQ;
-  // dQ: K_j in K slot j % kKRing, V_j in V slot j % kVRing
-  auto sK = [&](int i) -> uint32_t { return sbase + C::kOffRing + i * C::kTileBytes; };
-  auto sV = [&](int i) -> uint32_t { return sbase + C::kOffRing + (C::kKRing + i) * C::kTileBytes; };
-  auto k_full = [&](int t) { return ring_full(t % C::kKRing); };
-  auto k_empty = [&](int t) { return ring_empty(t % C::kKRing); };
-  auto v_full = [&](int t) { return ring_full(C::kKRing + t % C::kVRing); };
-  auto v_empty = [&](int t) { return ring_empty(C::kKRing + t % C::kVRing); };
+  // step t's ring-A tile sits in slot t % kARing, its ring-B tile in slot
+  // t % kBRing
+  auto sA = [&](int t) -> uint32_t { return sbase + C::kOffRing + (t % C::kARing) * C::kTileBytes; };
+  auto sB = [&](int t) -> uint32_t {
+    return sbase + C::kOffRing + (C::kARing + t % C::kBRing) * C::kTileBytes;
+  };
+  auto a_full = [&](int t) { return ring_full(t % C::kARing); };
+  auto a_empty = [&](int t) { return ring_empty(t % C::kARing); };
+  auto b_full = [&](int t) { return ring_full(C::kARing + t % C::kBRing); };
+  auto b_empty = [&](int t) { return ring_empty(C::kARing + t % C::kBRing); };
   const uint32_t acc_full = bar(C::kBarAcc);
   const uint32_t drain_bar = bar(C::kBarDrain);
   // fixed pair: [0] K or Q, [1] V or dO; ring slot i: [0] Q or K, [1] dO or V
   auto sFixed = [&](int w) -> uint32_t { return sbase + C::kOffFixed + w * C::kTileBytes; };
-  auto sRing = [&](int i, int w) -> uint32_t {
-    return sbase + C::kOffRing + (2 * i + w) * C::kTileBytes;
-  };
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
@@ -240,14 +242,13 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
 
   const CUtensorMap* fixed0 = DKDV ? &tmK : &tmQ;
   const CUtensorMap* fixed1 = DKDV ? &tmV : &tmDO;
-  const CUtensorMap* ring0 = DKDV ? &tmQ : &tmK;
-  const CUtensorMap* ring1 = DKDV ? &tmDO : &tmV;
+  const CUtensorMap* ringA = DKDV ? &tmQ : &tmK;
+  const CUtensorMap* ringB = DKDV ? &tmDO : &tmV;
 
-  if (warp == 0 || (!DKDV && warp == 3)) {
+  if (warp == 0 || warp == 3) {
     // ----------------------------------------------------------- producers
-    // Warp 0 loads the fixed pair, then (dK/dV) the ring of (Q_i, dO_i)
-    // pairs or (dQ) the K ring; in the dQ kernel warp 3 loads the V ring,
-    // each at its own pace.
+    // Warp 0 loads the fixed pair, then ring A; warp 3 loads ring B.  Each
+    // runs at its own pace.
     if (lane == 0 && n_steps > 0) {
       if (warp == 0) {
         ptx::mbar_arrive_expect_tx(fixed_full, 2 * C::kTileBytes);
@@ -256,35 +257,28 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
           ptx::tma_load_3d(sFixed(1) + h * C::kHalfBytes, fixed1, fixed_full, h * 64, r0, bh);
         }
       }
-      // one ring: pairs (dK/dV), K tiles or V tiles (dQ)
-      const bool is_v = !DKDV && warp == 3;
-      const int depth = DKDV ? C::kRing : (is_v ? C::kVRing : C::kKRing);
-      const int per_slot = DKDV ? 2 : 1;  // tiles per slot
-      auto full_of = [&](int t) { return DKDV ? ring_full(t % C::kRing) : (is_v ? v_full(t) : k_full(t)); };
-      auto empty_of = [&](int t) { return DKDV ? ring_empty(t % C::kRing) : (is_v ? v_empty(t) : k_empty(t)); };
-      auto dst_of = [&](int t, int w) -> uint32_t {
-        return DKDV ? sRing(t % C::kRing, w) : (is_v ? sV(t % C::kVRing) : sK(t % C::kKRing));
-      };
-      auto map_of = [&](int w) -> const CUtensorMap* { return DKDV ? (w ? ring1 : ring0) : (is_v ? &tmV : &tmK); };
+      const bool is_b = warp == 3;
+      const int depth = is_b ? C::kBRing : C::kARing;
+      const CUtensorMap* map = is_b ? ringB : ringA;
+      auto full_of = [&](int t) { return is_b ? b_full(t) : a_full(t); };
       int t = 0;
       bool ok = true;
       for (; t < n_steps; ++t) {
         const int use = t / depth;
-        if (use > 0 && !wait_one(empty_of(t), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
+        if (use > 0 && !wait_one(is_b ? b_empty(t) : a_empty(t), (use - 1) & 1, ctl, kSiteProducerEmpty)) {
           ok = false;
           break;
         }
         const int y = (t_begin + t) * C::kBlock;
-        ptx::mbar_arrive_expect_tx(full_of(t), per_slot * C::kTileBytes);
-        for (int w = 0; w < per_slot; ++w)
-          for (int h = 0; h < C::kHalves; ++h)
-            ptx::tma_load_3d(dst_of(t, w) + h * C::kHalfBytes, map_of(w), full_of(t), h * 64, y, bh);
-        // warm L2 one ring's depth ahead (two steps for the one-slot V ring)
+        const uint32_t dst = is_b ? sB(t) : sA(t);
+        ptx::mbar_arrive_expect_tx(full_of(t), C::kTileBytes);
+        for (int h = 0; h < C::kHalves; ++h)
+          ptx::tma_load_3d(dst + h * C::kHalfBytes, map, full_of(t), h * 64, y, bh);
+        // warm L2 one ring's depth ahead (two steps for a one-slot ring)
         const int ahead = t + max(depth, 2);
         if (ahead < n_steps) {
           const int y2 = (t_begin + ahead) * C::kBlock;
-          for (int w = 0; w < per_slot; ++w)
-            for (int h = 0; h < C::kHalves; ++h) ptx::tma_prefetch_3d(map_of(w), h * 64, y2, bh);
+          for (int h = 0; h < C::kHalves; ++h) ptx::tma_prefetch_3d(map, h * 64, y2, bh);
         }
       }
       if (!ok) {
@@ -347,69 +341,62 @@ __global__ void __launch_bounds__(BwdCfg<D>::kThreads, 1)
     // read those columns before it signals.  No barrier can complete two
     // phases ahead of its waiter: each next-but-one phase needs an action
     // that follows the waiter's observation of the current one.
-    auto ring_wait = [&](int t) {
-      return wait_warp(ring_full(t % C::kRing), (t / C::kRing) & 1, ctl, kSiteMmaKV);
+    auto a_wait = [&](int t) {
+      const bool r = wait_warp(a_full(t), (t / C::kARing) & 1, ctl, kSiteMmaKV);
+      if (r) ptx::tc_fence_after();
+      return r;
     };
-    if constexpr (DKDV) {
-      if (ok && (ok = ring_wait(0))) {
-        ptx::tc_fence_after();
-        issue_scores(tS, sFixed(0), sRing(0, 0));                // S^T = K Q_0^T
-        commit(s_full);
-        issue_scores(tmem + C::kColP2, sFixed(1), sRing(0, 1));  // dP^T = V dO_0^T
-        commit(dp_full(0));
-      }
-    } else {
-      if (ok && (ok = wait_warp(k_full(0), 0, ctl, kSiteMmaKV))) {
-        ptx::tc_fence_after();
-        issue_scores(tS, sFixed(0), sK(0));  // S = Q K_0^T
-        commit(s_full);
-      }
-      if (ok && (ok = wait_warp(v_full(0), 0, ctl, kSiteMmaKV))) {
-        ptx::tc_fence_after();
-        issue_scores(tmem + p2_col(0), sFixed(1), sV(0));  // dP = dO V_0^T
-        commit(dp_full(0));
-        commit(v_empty(0));
-      }
+    auto b_wait = [&](int t) {
+      const bool r = wait_warp(b_full(t), (t / C::kBRing) & 1, ctl, kSiteMmaKV);
+      if (r) ptx::tc_fence_after();
+      return r;
+    };
+    // prologue: step 0's scores and second product
+    if (ok && (ok = a_wait(0))) {
+      issue_scores(tS, sFixed(0), sA(0));  // S^T = K Q_0^T  |  S = Q K_0^T
+      commit(s_full);
+    }
+    if (ok && (ok = b_wait(0))) {
+      issue_scores(tmem + p2_col(0), sFixed(1), sB(0));  // dP^T = V dO_0^T  |  dP = dO V_0^T
+      commit(dp_full(0));
+      if constexpr (!DKDV) commit(b_empty(0));  // V_0 is read by dP_0 alone
     }
     for (int t = 0; t < n_steps && ok; ++t) {
-      const int slot = t % C::kRing;
-      const int nslot = (t + 1) % C::kRing;
       const bool more = t + 1 < n_steps;
       if (!(ok = wait_warp(p_ready, t & 1, ctl, kSiteMmaP))) break;
       ptx::tc_fence_after();
-      if constexpr (!DKDV) {
+      if constexpr (DKDV) {
+        issue_acc(tAcc0, tS + C::kPackOff, sB(t), t == 0);  // dV += P^T dO_t
+        commit(b_empty(t));  // dO_t: read by dP^T_t and dV_t, both issued
+        if (more) {
+          if (!(ok = a_wait(t + 1))) break;
+          issue_scores(tS, sFixed(0), sA(t + 1));  // S^T_{t+1}
+          commit(s_full);
+        }
+        if (!(ok = wait_warp(ds_ready(0), t & 1, ctl, kSiteMmaP))) break;
+        ptx::tc_fence_after();
+        issue_acc(tAcc1, tmem + C::kColP2 + C::kPackOff, sA(t), t == 0);  // dK += dS^T Q_t
+        commit(a_empty(t));
+        if (more) {
+          if (!(ok = b_wait(t + 1))) break;
+          issue_scores(tmem + C::kColP2, sFixed(1), sB(t + 1));  // dP^T_{t+1}
+          commit(dp_full(0));
+        }
+      } else {
         if (more) {
           const int u = t + 1;
-          if (!(ok = wait_warp(k_full(u), (u / C::kKRing) & 1, ctl, kSiteMmaKV))) break;
-          ptx::tc_fence_after();
-          issue_scores(tS, sFixed(0), sK(u % C::kKRing));  // S_{t+1}
+          if (!(ok = a_wait(u))) break;
+          issue_scores(tS, sFixed(0), sA(u));  // S_{t+1}
           commit(s_full);
-          if (!(ok = wait_warp(v_full(u), (u / C::kVRing) & 1, ctl, kSiteMmaKV))) break;
-          ptx::tc_fence_after();
-          issue_scores(tmem + p2_col(u), sFixed(1), sV(u % C::kVRing));  // dP_{t+1}
+          if (!(ok = b_wait(u))) break;
+          issue_scores(tmem + p2_col(u), sFixed(1), sB(u));  // dP_{t+1}
           commit(dp_full(p2_buf(u)));
-          commit(v_empty(u));
+          commit(b_empty(u));
         }
         if (!(ok = wait_warp(ds_ready(p2_buf(t)), p2_par(t), ctl, kSiteMmaP))) break;
         ptx::tc_fence_after();
-        issue_acc(tAcc0, tmem + p2_col(t) + C::kPackOff, sK(t % C::kKRing), t == 0);  // dQ += dS K_t
-        commit(k_empty(t));
-        continue;
-      }
-      issue_acc(tAcc0, tS + C::kPackOff, sRing(slot, 1), t == 0);  // dV += P^T dO_t
-      if (more) {
-        if (!(ok = ring_wait(t + 1))) break;
-        ptx::tc_fence_after();
-        issue_scores(tS, sFixed(0), sRing(nslot, 0));
-        commit(s_full);
-      }
-      if (!(ok = wait_warp(ds_ready(0), t & 1, ctl, kSiteMmaP))) break;
-      ptx::tc_fence_after();
-      issue_acc(tAcc1, tmem + C::kColP2 + C::kPackOff, sRing(slot, 0), t == 0);  // dK += dS^T Q_t
-      commit(ring_empty(slot));
-      if (more) {
-        issue_scores(tmem + C::kColP2, sFixed(1), sRing(nslot, 1));  // dP^T_{t+1}
-        commit(dp_full(0));
+        issue_acc(tAcc0, tmem + p2_col(t) + C::kPackOff, sA(t), t == 0);  // dQ += dS K_t
+        commit(a_empty(t));
       }
     }
     if (ok) commit(acc_full);

@@ -110,3 +110,34 @@ def test_bwd_tiles_fastest_launch_order(causal):
     got = run_bwd(q, k, v, do, causal)
     ref = oracle.attention_bwd(q, k, v, do, scale_for(64), causal)
     check(got, ref, f"N4224 causal={causal}")
+
+
+def test_bwd_full_workload_one_head():
+    """The whole B=1, H=32, N=16384, d=128 causal workload that the backward
+    benchmark times, in the same launch configuration: every gradient finite,
+    and one head's dQ, dK, dV compared in full with the oracle's."""
+    import torch
+
+    import head_attention_forward_gb300 as mha
+    c = synth.CONFIGS["cfg5"]
+    B, H, N, d, causal = c["B"], c["H"], c["N"], c["d"], c["causal"]
+    q, k, v = synth.qkv(c["seed"], B, H, N, d, c["sigma_qk"], c["sigma_v"])
+    do = synth.normal_bf16_c(c["seed"], 3, B * H * N * d).reshape(B, H, N, d)
+    scale = scale_for(d)
+    qd, kd, vd, dod = (to_device(x) for x in (q, k, v, do))
+    o = torch.empty_like(qd)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    mha.mha_fwd(qd, kd, vd, o, lse, B, H, N, d, scale, causal)
+    grads = [torch.full_like(qd, float("nan")) for _ in range(3)]
+    ws_bytes = mha.mha_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    mha.mha_bwd(qd, kd, vd, o, lse, dod, *grads, B, H, N, d, scale, causal, ws, ws_bytes)
+    rc, word = mha.mha_device_status()
+    assert rc == mha.MHA_OK, f"device status {rc} word {word:#x}"
+    for g in grads:
+        assert bool(torch.isfinite(g.float()).all())
+    h = 21
+    got = [bf16_to_f64(g[:, h:h + 1]) for g in grads]
+    one = [np.ascontiguousarray(x[:, h:h + 1]) for x in (q, k, v, do)]
+    ref = oracle.attention_bwd(*one, scale, causal)
+    check(got, ref, f"cfg5 head {h}")

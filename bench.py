@@ -36,6 +36,9 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
+# NVIDIA's dense bf16 figure for one GB300 (without 2:4 sparsity), reported
+# beside the measured denominators
+NOMINAL_BF16_TFLOPS = 2250.0
 METRIC = "attention fwd TFLOP/s and % of GB300 bf16 tensor peak, per (B,H,N,d,causal)"
 UNIT = "TFLOP/s"
 FALLBACK_PEAK_TFLOPS = 1900.0  # used only when MEASURED_PEAKS.json is absent
@@ -659,6 +662,11 @@ def main():
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "pct_of_peak": 100.0 * value / world / peak,
             "pct_of_burst_peak": 100.0 * value / world / peak_burst,
+            "pct_of_nominal_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
+            "median_launch_ms": statistics.median(per_launch_ms),
+            # exponentials the softmax evaluates per second (one per visible
+            # score, counted like the FLOPs: B*H*N^2, halved when causal)
+            "exp2_per_s": flops / (4.0 * d) / (statistics.median(per_launch_ms) / 1e3),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "peak_source": peak_src,
                          "peak_burst": peak_burst, "frac_burst": achieved / peak_burst,

@@ -19,14 +19,16 @@
 // per query tile in the other), so no partial sum goes through global
 // atomics.
 //
-// Both kernels share the forward kernel's shape: warp 0 feeds tiles with TMA
-// through mbarrier-guarded shared-memory slots, warp 1 allocates TMEM and
-// runs the tcgen05.mma issue loop (whole warp, one elected lane issues),
-// and warps 4-11 do the elementwise work, two threads per row of the tile
-// (one TMEM lane): warps 4-7 take columns 0-63 and warps 8-11 columns
-// 64-127.  The recomputed P needs no row-wise reduction (it comes from the
-// saved LSE), so the two halves never exchange anything.  Warps 2-3 only
-// keep warps 4-11 on TMEM lane quarters.  P^T is written back to TMEM as
+// Both kernels share the forward kernel's shape.  Warp 0 loads the CTA's
+// fixed pair of tiles and feeds ring A (the score product's operand: Q_i for
+// dK/dV, K_j for dQ) with TMA; warp 3 feeds ring B (the second product's
+// operand: dO_i, V_j), each ring a set of mbarrier-guarded shared-memory
+// slots.  Warp 1 allocates TMEM and runs the tcgen05.mma issue loop (whole
+// warp, one elected lane issues).  Warps 4-11 do the elementwise work, two
+// threads per row of the tile (one TMEM lane): warps 4-7 take columns 0-63
+// and warps 8-11 columns 64-127.  The recomputed P needs no row-wise
+// reduction (it comes from the saved LSE), so the two halves never exchange
+// anything.  Warp 2 only keeps warps 4-11 on TMEM lane quarters.  P^T is written back to TMEM as
 // bf16 over S^T, and dS (dS^T) over dP (dP^T), each packed into columns
 // 32-95 of its 128: every warp then overwrites only score columns it has
 // already read itself.  Each is the A operand of a later MMA straight from

@@ -43,10 +43,10 @@
 // Split mode (SPLIT) serves split-KV decoding, a few queries against a long
 // key sequence: work tiles are (head, key split) pairs that warp 0 hands out
 // at run time; the queries (at most 32) sit in the first softmax warp of
-// stage 0 and the other softmax warps have no work; the scores are
-// double-buffered in both stages' S columns, so S_{j+1} is computed while
-// the softmax works on S_j; each split writes an fp32 partial output and
-// its LSE for a merge kernel.  PAGED gathers each 128-key tile of a paged
+// each stage and the other softmax warps have no work; a split's K/V tiles
+// alternate between the stages, so the two stages' softmax warps work on
+// consecutive tiles at once; each stage writes an fp32 partial output and
+// its LSE for a merge kernel (two partials per split).  PAGED gathers each 128-key tile of a paged
 // K/V cache from page-sized TMA boxes named by a block table.
 //
 // Every mbarrier wait is bounded (clock64 budget).  A wait that runs out
@@ -73,11 +73,12 @@ struct FwdParams {
   int BH;              // batch * heads; work tiles are (bh, m-block) pairs
   // split mode only: Nq <= 32 queries per head (one Q tile, rows past Nq
   // read as zeros) against Nk keys cut into num_splits runs of tiles_per_split
-  // K/V tiles; work tiles are (bh, split) pairs and each writes an fp32
-  // partial output normalised by its own sum, plus its log-sum-exp
+  // K/V tiles; work tiles are (bh, split) pairs, and each stage writes an
+  // fp32 partial output for its half of the split's tiles, normalised by its
+  // own sum, plus its log-sum-exp
   int Nq, Nk, num_splits, tiles_per_split;
-  float* o_part;       // [BH, num_splits, Nq, D]
-  float* lse_part;     // [BH, num_splits, Nq]
+  float* o_part;       // [BH, 2 * num_splits, Nq, D] (one partial per split and stage)
+  float* lse_part;     // [BH, 2 * num_splits, Nq]
   float scale_log2;    // scale * log2(e)
   // paged mode only (split mode over a paged cache): key t of batch entry
   // b = bh / num_heads is row t % page_size of cache block
@@ -162,10 +163,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   auto tiles_for = [&](int row0) {
     return row0 >= N ? 0 : (CAUSAL ? min(n_tiles, row0 / C::kBlockN + 1) : n_tiles);
   };
-  // a work tile: head, first query row, K/V tiles per stage, keys of the
-  // head (split mode: n0 is 0 for a split past them)
+  // a work tile: head, first query row, K/V tiles per stage and in all,
+  // keys of the head (split mode: nkv is 0 for a split past them)
   struct Tile {
-    int bh, m0, n0, n1, kv_begin, split, nk;
+    int bh, m0, n0, n1, nkv, kv_begin, split, nk;
   };
   // split mode: tile u is split u / BH of head bh = u % BH, so the heads of
   // one batch entry (bh = b * heads + h) are adjacent.  Every tile runs on
@@ -180,8 +181,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     t.kv_begin = t.split * p.tiles_per_split;
     t.m0 = 0;
     t.nk = keys_of(t.bh);
-    t.n0 = max(0, min(p.tiles_per_split, (t.nk + C::kBlockN - 1) / C::kBlockN - t.kv_begin));
-    t.n1 = 0;
+    // the split's K/V tiles alternate between the stages: stage s takes
+    // tiles j = s mod 2
+    t.nkv = max(0, min(p.tiles_per_split, (t.nk + C::kBlockN - 1) / C::kBlockN - t.kv_begin));
+    t.n0 = (t.nkv + 1) / 2;
+    t.n1 = t.nkv / 2;
   };
   // square mode: the k-th tile of this CTA in the static order
   auto tile_at = [&](int k, Tile& t) -> bool {
@@ -196,6 +200,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     t.m0 = mblk * 256;
     t.n0 = tiles_for(t.m0);
     t.n1 = tiles_for(t.m0 + C::kBlockM);
+    t.nkv = max(t.n0, t.n1);  // both stages read the same K/V tiles
     return true;
   };
 
@@ -260,10 +265,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       ptx::mbar_init(kv_full(i), 1);
       ptx::mbar_init(kv_empty(i), 1);
     }
-    // one elected arrive per softmax warp of the stage; split mode: per
-    // warp of stage 0 that holds one of the Nq query rows (the other softmax
-    // warps have no work there and wait at the final barrier)
-    const int p_arrivals = SPLIT ? min(4, (p.Nq + 31) / 32) : 4;
+    // one elected arrive per softmax warp of the stage; split mode: the
+    // Nq <= 32 query rows lie in the first warp of each stage, and the other
+    // softmax warps have no work there and wait at the final barrier
+    const int p_arrivals = SPLIT ? 1 : 4;
     for (int s = 0; s < 2; ++s) {
       ptx::mbar_init(s_full(s), 1);
       ptx::mbar_init(p_ready(s), p_arrivals);
@@ -273,7 +278,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     ptx::mbar_init(tail_bar, 1);
     for (int i = 0; i < C::kTileRing; ++i) {
       ptx::mbar_init(tile_full(i), 1);
-      ptx::mbar_init(tile_empty(i), 2 + p_arrivals);  // one arrive per consumer warp
+      ptx::mbar_init(tile_empty(i), 2 + 2 * p_arrivals);  // one arrive per consumer warp
     }
     *abort_flag = 0;
     ptx::fence_barrier_init();
@@ -363,7 +368,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     }
     int blk_next = (PAGED && have) ? block_of(tl, 0) : 0;
     for (int k = 0; ok && have; ++k) {
-      const int n_kv = max(tl.n0, tl.n1);
+      const int n_kv = tl.nkv;
       // split mode: the next tile is drawn once this one's last copy is
       // issued (drawing it two K/V tiles earlier measured the same)
       int u_next = total;
@@ -461,7 +466,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       int kq = 0;  // work tiles with K/V tiles so far: the sets go to those only
       bool ok = true;
       for (int k = 0; ok && take_tile(k, tl, ok, false, kSiteProducerEmpty); ++k) {
-        if (max(tl.n0, tl.n1) == 0) continue;  // a split past the head's keys
+        if (tl.nkv == 0) continue;  // a split past the head's keys
         // the set's previous tile (kq - kQSets) must be done with it
         const int prev = kq - kQS;
         if (prev >= 0 && !wait_one(q_empty(q_set(prev)), q_par(prev), ctl, kSiteProducerEmpty)) {
@@ -545,21 +550,20 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       int kq = 0;                // work tiles with K/V tiles so far (Q set uses)
       for (int k = 0; ok && take_tile(k, tl, ok, true, kSiteMmaQ); ++k) {
         auto n_s = [&](int s) { return s ? tl.n1 : tl.n0; };
-        const int n_kv = max(tl.n0, tl.n1);
+        const int n_kv = tl.nkv;
         if (n_kv == 0) continue;  // a split past the head's keys
         const int qb = q_set(kq);
         if (!(ok = wait_warp(q_full(qb), q_par(kq), ctl, kSiteMmaQ))) break;
         ++kq;
         if constexpr (SPLIT) {
-          // One stage, its scores double-buffered in the S columns of both
-          // stages: S_{j+1} = Q K_{j+1}^T is issued before P_j V_j, so the
-          // softmax of tile j+1 starts as soon as that of tile j is done
-          // instead of waiting for P_j V_j and then S_{j+1}.  (The MMAs run
-          // in issue order, so S_{j+2} overwrites P_j only after P_j V_j.)
-          // o_full(0) completes after every P_j V_j: the softmax, whose
-          // rescale of O may otherwise meet P_{j-1} V_{j-1} still running,
-          // waits on it at every tile after the first and at the epilogue.
-          const int n = tl.n0;
+          // The split's K/V tiles alternate between the stages (stage s
+          // takes tiles j = s mod 2, with its own S columns, O accumulator
+          // and softmax warp), and S_{j+1} is issued before P_j V_j: the two
+          // softmax warps work on consecutive tiles at the same time, and
+          // neither waits for P V before its next scores.  The MMAs run in
+          // issue order, so S_{j+2} overwrites P_j only after P_j V_j, and
+          // when a stage sees S_j complete its P_{j-2} V_{j-2} is done too.
+          const int n = tl.nkv;
           const int t0 = t;  // ring position of K_0
           auto slot_of = [&](int pos) { return pos % C::kStages; };
           auto par_of = [&](int pos) { return static_cast<uint32_t>((pos / C::kStages) & 1); };
@@ -574,13 +578,16 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
               if (j + 2 == n) commit(q_empty(qb));  // this tile's Q is no longer read
             }
             if (j < 0) continue;
+            const int st = j & 1;
             const int vp = t0 + 2 * j + 1;  // V_j
-            if (!(ok = wait_warp(p_ready(0), pr[0] & 1, ctl, kSiteMmaP))) break;
-            ++pr[0];
+            // (pr indexed with constants only, so that it stays in registers)
+            const int seen = st ? pr[1] : pr[0];
+            if (!(ok = wait_warp(p_ready(st), seen & 1, ctl, kSiteMmaP))) break;
+            if (st) ++pr[1]; else ++pr[0];
             if (!(ok = wait_warp(kv_full(slot_of(vp)), par_of(vp), ctl, kSiteMmaKV))) break;
             ptx::tc_fence_after();
-            issue_pv_from(j & 1, 0, slot_of(vp), j == 0);
-            commit(o_full(0));
+            issue_pv(st, slot_of(vp), j < 2);
+            if (j >= n - 2) commit(o_full(st));  // the stage's last tile of this split
             commit(kv_empty(slot_of(vp)));
           }
           t = t0 + 2 * n;
@@ -641,38 +648,35 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     const uint32_t t_o = tmem + lane_off + (s ? C::kColO1 : C::kColO0);
     const float sl2 = p.scale_log2;
     bool ok = true;
-    int sf[2] = {0, 0};  // s_full completions consumed, per S buffer
+    int sf = 0;  // s_full completions consumed
     int of = 0;  // o_full completions consumed
     Tile tl;
-    // split mode: stage 1, and every warp whose 32 rows all lie past the
-    // Nq queries, has no work; such warps go straight to the final barrier
-    // (not even polling the tile ring), which leaves their SM
+    // split mode: the Nq <= 32 query rows lie in the first warp of each
+    // stage; the other softmax warps have no work and go straight to the
+    // final barrier (not even polling the tile ring), which leaves their SM
     // sub-partitions to the warps that share them
-    const bool idle = SPLIT && (s == 1 || wq * 32 >= p.Nq);
+    const bool idle = SPLIT && wq > 0;
     for (int k = 0; !idle && ok && take_tile(k, tl, ok, true, kSiteSoftmaxS); ++k) {
       const int m0 = tl.m0;
       const int n = s ? tl.n1 : tl.n0;
-      const int q_idx = m0 + s * C::kBlockM + row;
+      const int q_idx = SPLIT ? row : m0 + s * C::kBlockM + row;
       float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale
       float l_run = 0.f;   // row sum of exp2 terms (fp32), for the LSE
       float lr_run = 0.f;  // the same over the bf16-rounded terms, for O
       for (int j = 0; j < n; ++j) {
-        // S buffer of this tile: the stage's own, or in split mode the two
-        // stages' S columns in turn
-        const int sb = SPLIT ? (j & 1) : s;
-        const uint32_t t_sj = SPLIT ? tmem + lane_off + (sb ? C::kColS1 : C::kColS0) : t_s;
-        if (!wait_warp(s_full(sb), sf[sb] & 1, ctl, kSiteSoftmaxS)) {
+        if (!wait_warp(s_full(s), sf & 1, ctl, kSiteSoftmaxS)) {
           ok = false;
           break;
         }
-        ++sf[sb];
+        ++sf;
         ptx::tc_fence_after();
         uint32_t raw[128];
-        ptx::tmem_ld_x128(t_sj, raw);
+        ptx::tmem_ld_x128(t_s, raw);
         float x[128];
 #pragma unroll
         for (int cc = 0; cc < 128; ++cc) x[cc] = __uint_as_float(raw[cc]);
-        const int kv0 = (tl.kv_begin + j) * C::kBlockN;
+        // this stage's j-th K/V tile (split mode: tile 2j + s of the split)
+        const int kv0 = (tl.kv_begin + (SPLIT ? 2 * j + s : j)) * C::kBlockN;
         const int nk = tl.nk;  // keys of this head
         // square: query i sees keys 0..i; split: query i of Nq sees keys
         // 0..nk-Nq+i (the queries are the last Nq positions)
@@ -719,19 +723,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             sumr[(2 * i) & 3] = ptx::add_bf16_lo(pk[i], sumr[(2 * i) & 3]);
             sumr[(2 * i + 1) & 3] = ptx::add_bf16_hi(pk[i], sumr[(2 * i + 1) & 3]);
           }
-          ptx::tmem_st_x16(t_sj + c4 * 16, pk);
+          ptx::tmem_st_x16(t_s + c4 * 16, pk);
         }
         l_run = l_run * alpha + ((sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y));
         lr_run = lr_run * alpha + ((sumr[0] + sumr[1]) + (sumr[2] + sumr[3]));
-        if (SPLIT && j > 0) {
-          // P_{j-1} V_{j-1} was issued after S_j: it lands before O is touched
-          if (!wait_warp(o_full(0), of & 1, ctl, kSiteSoftmaxO)) {
-            ok = false;
-            break;
-          }
-          ++of;
-          ptx::tc_fence_after();
-        }
         // correction: bring O(s) to the new max before P_j(s) V_j lands on it
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
@@ -748,7 +743,23 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(p_ready(s));
       }
-      if (!ok || n == 0) continue;
+      if (!ok) continue;
+      if constexpr (SPLIT) {
+        if (n == 0) {
+          // a one-tile split leaves stage 1 without keys: an empty partial
+          // (the merge gives it zero weight; its O must still be finite)
+          if (q_idx < p.Nq) {
+            const size_t prow =
+                (static_cast<size_t>(tl.bh) * 2 * p.num_splits + 2 * tl.split + s) * p.Nq + q_idx;
+            float4* dst = reinterpret_cast<float4*>(p.o_part + prow * D);
+#pragma unroll
+            for (int v4 = 0; v4 < D / 4; ++v4) dst[v4] = make_float4(0.f, 0.f, 0.f, 0.f);
+            p.lse_part[prow] = -INFINITY;
+          }
+          continue;
+        }
+      }
+      if (n == 0) continue;
       if (!wait_warp(o_full(s), of & 1, ctl, kSiteSoftmaxO)) {
         ok = false;
         break;
@@ -762,12 +773,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
       const float lse_row = l_run > 0.f ? (m_fin + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;
       if constexpr (SPLIT) {
-        // fp32 partial row of this split, normalised by its own sum.  The
+        // fp32 partial row of this stage's half of the split, normalised by
+        // its own sum: each split gives two partials, 2 * split + stage.  The
         // TMEM loads are warp-collective: every lane issues them, only rows
         // below Nq store.
         const bool live = q_idx < p.Nq;
         const size_t prow =
-            (static_cast<size_t>(tl.bh) * p.num_splits + tl.split) * p.Nq + (live ? q_idx : 0);
+            (static_cast<size_t>(tl.bh) * 2 * p.num_splits + 2 * tl.split + s) * p.Nq + (live ? q_idx : 0);
         float* orow = p.o_part + prow * D;
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) {

@@ -30,10 +30,12 @@ struct Plan {
   size_t o_part_bytes = 0, lse_part_bytes = 0, lse_off = 0, counter_off = 0, total = 0;
 };
 
-// Split count and workspace layout: o_part fp32 [BH, splits, Nq, d], then
-// (16-byte aligned) lse_part fp32 [BH, splits, Nq], then (16-byte aligned)
-// the partial pass's work-tile counter (one int in 16 bytes).  A split is a
-// run of tiles_per_split 128-key tiles.
+// Split count and workspace layout: o_part fp32 [BH, 2 * splits, Nq, d],
+// then (16-byte aligned) lse_part fp32 [BH, 2 * splits, Nq], then (16-byte
+// aligned) the partial pass's work-tile counter (one int in 16 bytes).  A
+// split is a run of tiles_per_split 128-key tiles, and gives two partials:
+// the partial pass alternates its tiles between two stages.
+constexpr int kPartsPerSplit = 2;
 Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits) {
   Plan pl;
   const int tiles = (Nk + kTileKeys - 1) / kTileKeys;
@@ -42,8 +44,8 @@ Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits) {
   want = std::max(1, std::min(want, tiles));
   pl.tiles_per_split = (tiles + want - 1) / want;
   pl.splits = (tiles + pl.tiles_per_split - 1) / pl.tiles_per_split;
-  pl.o_part_bytes = static_cast<size_t>(BH) * pl.splits * Nq * d * 4;
-  pl.lse_part_bytes = static_cast<size_t>(BH) * pl.splits * Nq * 4;
+  pl.o_part_bytes = static_cast<size_t>(BH) * kPartsPerSplit * pl.splits * Nq * d * 4;
+  pl.lse_part_bytes = static_cast<size_t>(BH) * kPartsPerSplit * pl.splits * Nq * 4;
   pl.lse_off = (pl.o_part_bytes + 15) & ~static_cast<size_t>(15);
   pl.counter_off = (pl.lse_off + pl.lse_part_bytes + 15) & ~static_cast<size_t>(15);
   pl.total = pl.counter_off + 16;
@@ -61,9 +63,9 @@ int check_shape(int B, int H, int Nq, int Nk, int d, int num_splits) {
   return MHA_OK;
 }
 
-// Paged caches: what the merge needs to count each entry's splits.
+// Paged caches: what the merge needs to count each entry's partials.
 struct PagedSplits {
-  const int* seq_lens = nullptr;  // null: every head has all the splits
+  const int* seq_lens = nullptr;  // null: every head has all the partials
   int num_heads = 1, max_keys = 0;
   long long split_keys = 1;       // keys per split
 };
@@ -77,12 +79,13 @@ int launch_merge(const float* o_part, const float* lse_part, void* o, float* lse
   mcfg.stream = st;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
   cudaError_t err;
+  const int parts = kPartsPerSplit * splits;
   if (d == 64)
-    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, o_part, lse_part, ob, lse, Nq, splits,
-                             ps.seq_lens, ps.num_heads, ps.split_keys, ps.max_keys);
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<64>, o_part, lse_part, ob, lse, Nq, parts,
+                             kPartsPerSplit, ps.seq_lens, ps.num_heads, ps.split_keys, ps.max_keys);
   else
-    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, o_part, lse_part, ob, lse, Nq, splits,
-                             ps.seq_lens, ps.num_heads, ps.split_keys, ps.max_keys);
+    err = cudaLaunchKernelEx(&mcfg, mha::splitkv_merge_kernel<128>, o_part, lse_part, ob, lse, Nq, parts,
+                             kPartsPerSplit, ps.seq_lens, ps.num_heads, ps.split_keys, ps.max_keys);
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 

@@ -29,21 +29,24 @@ constexpr int kSplitMaxQ = 16;  // queries per call (decode-sized blocks)
 template <int D>
 __global__ void __launch_bounds__(D) splitkv_merge_kernel(const float* o_part, const float* lse_part,
                                                          __nv_bfloat16* o, float* lse, int Nq,
-                                                         int num_splits, const int* seq_lens,
-                                                         int num_heads, long long split_keys,
-                                                         int max_keys) {
+                                                         int num_splits, int parts_per_split,
+                                                         const int* seq_lens, int num_heads,
+                                                         long long split_keys, int max_keys) {
   static_assert(D % 32 == 0, "whole warps");
   __shared__ float red[D / 32];
   __shared__ float w_s[D];
   const int qi = blockIdx.x, bh = blockIdx.y, c = threadIdx.x;
   const int lane = c & 31, warp = c >> 5;
   const size_t base = static_cast<size_t>(bh) * num_splits;
-  // paged caches: an entry has only the splits that hold some of its keys
-  // (the partial pass may skip the others and leave their slots unwritten)
+  // num_splits partials per head, parts_per_split of them per key split.
+  // Paged caches: an entry has only the partials of the splits that hold
+  // some of its keys (the partial pass skips the others and leaves their
+  // slots unwritten).
   int ns = num_splits;
   if (seq_lens) {
     const long long nk = max(0, min(seq_lens[bh / num_heads], max_keys));
-    ns = static_cast<int>(min(static_cast<long long>(num_splits), (nk + split_keys - 1) / split_keys));
+    ns = static_cast<int>(min(static_cast<long long>(num_splits),
+                              parts_per_split * ((nk + split_keys - 1) / split_keys)));
   }
   auto lse_of = [&](int s) { return lse_part[(base + s) * Nq + qi]; };
   // the largest split LSE

@@ -94,9 +94,9 @@ def test_kv_workspace_size_is_pure():
     import head_attention_forward_gb300 as mha
     a = mha.mha_fwd_kv_workspace_size(2, 8, 1, 32768, 128, 0)
     assert a > 0 and a == mha.mha_fwd_kv_workspace_size(2, 8, 1, 32768, 128, 0)
-    # explicit split count: o_part (fp32) + 16-byte aligned lse_part + the
-    # 16-byte slot of the work-tile counter
-    assert mha.mha_fwd_kv_workspace_size(1, 1, 4, 1000, 64, 2) == 2 * 4 * 64 * 4 + 2 * 4 * 4 + 16
+    # explicit split count: two fp32 partials per split (o_part, then the
+    # 16-byte aligned lse_part) + the 16-byte slot of the work-tile counter
+    assert mha.mha_fwd_kv_workspace_size(1, 1, 4, 1000, 64, 2) == 2 * 2 * 4 * 64 * 4 + 2 * 2 * 4 * 4 + 16
     assert mha.mha_fwd_kv_workspace_size(1, 1, 17, 100, 64, 0) == 0   # Nq > 16
     assert mha.mha_fwd_kv_workspace_size(1, 1, 1, 100, 96, 0) == 0    # bad d
     assert mha.mha_fwd_kv_workspace_size(0, 1, 1, 100, 64, 0) == 0    # empty

@@ -1,12 +1,16 @@
 """Benchmark of the fused attention forward on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-                    [--impl ours|reference] [--no-cpu-baseline]
+                    [--impl ours|reference] [--no-cpu-baseline] [--backward]
+                    [--e2e-steps E]
 
 One step is one attention forward pass (the whole hot path: Q/K/V tile
 loads, S = Q K^T, masked online softmax, O += P V, O/LSE epilogue) over one
 synthetic batch.  The default workload is the long-sequence causal case
 B=1, H=32, N=16384, d=128 ("cfg5"); other names are listed in synth.CONFIGS.
+The decode names (synth.DECODE_CONFIGS, synth.PAGED_CONFIGS) time the
+split-KV and paged paths against the HBM roofline instead, and --backward
+times mha_bwd on a forward workload.
 
 Metric: attention forward TFLOP/s, counting 4*B*H*N^2*d FLOPs per pass
 (half of that with the causal mask), aggregated over all ranks.  Rank 0

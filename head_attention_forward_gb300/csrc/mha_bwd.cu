@@ -132,7 +132,7 @@ int mha_bwd(const void* q, const void* k, const void* v, const void* o, const fl
     return MHA_ERR_CUDA;
 
   float* dsum = static_cast<float*>(workspace);
-  mha::BwdParams prm;
+  mha::BwdParams prm = {};
   prm.lse = lse;
   prm.dsum = dsum;
   prm.dq = static_cast<__nv_bfloat16*>(dq);

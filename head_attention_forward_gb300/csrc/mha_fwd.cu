@@ -303,7 +303,7 @@ int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
       !encode_map(&mv, v, static_cast<int>(BH), N, d, 128))
     return MHA_ERR_CUDA;
 
-  mha::FwdParams prm;
+  mha::FwdParams prm = {};
   prm.o = static_cast<__nv_bfloat16*>(o);
   prm.lse = lse;
   prm.status = status;

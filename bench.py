@@ -575,6 +575,19 @@ def main():
     if rc != mha.MHA_OK:
         raise RuntimeError(f"device status after timing: {rc} ({word:#x})")
 
+    # one launch right after L2 has been flushed (a 256 MB write), timed alone
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    cold_ms = []
+    for _ in range(3):
+        flush.fill_(1)
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        step()
+        c1.record(stream)
+        torch.cuda.synchronize(dev)
+        cold_ms.append(c0.elapsed_time(c1))
+    del flush
+
     flops = counted_flops(c)
     value = flops * args.steps * world / (total_ms / 1e3) / 1e12
     mean_launch_ms = statistics.mean(per_launch_ms)
@@ -668,6 +681,7 @@ def main():
             "pct_of_burst_peak": 100.0 * value / world / peak_burst,
             "pct_of_nominal_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
             "median_launch_ms": statistics.median(per_launch_ms),
+            "cold_launch_ms": statistics.median(cold_ms),  # after an L2 flush
             # exponentials the softmax evaluates per second (one per visible
             # score, counted like the FLOPs: B*H*N^2, halved when causal)
             "exp2_per_s": flops / (4.0 * d) / (statistics.median(per_launch_ms) / 1e3),

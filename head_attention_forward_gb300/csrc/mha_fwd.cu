@@ -126,6 +126,21 @@ bool encode_map(CUtensorMap* map, const void* base, int BH, int N, int d, int bo
 
 bool encode_paged_map(CUtensorMap* map, const void* base, int num_blocks, int H, int page_size,
                       int d, int box_rows) {
+  if (d == 128) {
+    // [block * heads + head][8-row group][d-half][row][64]: one box brings
+    // box_rows rows with both halves, each 8-row group's two 128-byte
+    // swizzle atoms side by side (the strides need not grow outward)
+    cuuint64_t dims[5] = {64, 8, 2, static_cast<cuuint64_t>(page_size / 8),
+                          static_cast<cuuint64_t>(num_blocks) * H};
+    cuuint64_t strides[4] = {256, 128, 2048, static_cast<cuuint64_t>(page_size) * 256};
+    cuuint32_t box[5] = {64, 8, 2, static_cast<cuuint32_t>(box_rows / 8), 1};
+    cuuint32_t estride[5] = {1, 1, 1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims,
+                          strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  }
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(page_size),
                         static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(num_blocks)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(d) * 2,

@@ -139,8 +139,11 @@ __device__ __forceinline__ int fwd_tile_of_round(int k, int c, int G) {
 // the Q buffers of both stages serve as two Q sets, and work tiles are
 // handed out at run time.
 // PAGED = true (with SPLIT): the same pass over a paged K/V cache, each
-// batch entry with its own key count; tmK / tmV are then 4-D maps
-// [blocks][heads][page rows][d] with boxes of min(page_size, 128) rows.
+// batch entry with its own key count; tmK / tmV then map the cache
+// [blocks][heads][page rows][d] with boxes of min(page_size, 128) rows: at
+// d = 64 as 4-D [blocks][heads][page rows][d]; at d = 128 as 5-D
+// [blocks * heads][8-row group][d-half][row][64], which brings both
+// d-halves of a box's rows in one copy.
 template <int D, bool CAUSAL, bool SPLIT = false, bool PAGED = false>
 __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     mha_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -227,6 +230,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   auto q_index = [](int b, int s) { return SPLIT ? b : 2 * b + s; };
   auto sQ = [&](int b, int s) -> uint32_t { return sbase + C::kOffQ + q_index(b, s) * C::kTileBytes; };
   auto sKV = [&](int i) -> uint32_t { return sbase + C::kOffKV + i * C::kTileBytes; };
+  // Layout of a K/V tile in shared memory: 8-key groups of 128-byte swizzle
+  // atoms.  Contiguous K/V: each d-half is a 16 KiB block of its own (groups
+  // 1 KiB apart).  Paged at d = 128: one copy per page brings both halves
+  // of its keys, so a group holds its two atoms side by side (halves 1 KiB
+  // apart, groups 2 KiB apart); the tensor core reads either through the
+  // same descriptors with these two strides.
+  constexpr bool kPairedHalves = PAGED && D == 128;
+  constexpr int kKVGroupBytes = kPairedHalves ? 2048 : 1024;
+  constexpr int kKVHalfBytes = kPairedHalves ? 1024 : C::kHalfBytes;
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffTmemSlot);
@@ -296,6 +308,9 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // split mode: the merge kernel may start on SMs this grid leaves (it
+  // waits for this grid's completion before reading any partial)
+  if (SPLIT && threadIdx.x == 0) ptx::griddep_launch_dependents();
 
   if (warp == 0) {
     // -------------------------------------------------- K/V producer
@@ -317,7 +332,10 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // a page past the entry's length reads as zeros (a block id past the
       // cache); pos < nk also keeps the table read inside its row
       if (lane >= chunks || pos >= w.nk) return p.num_blocks;
-      return p.block_table[static_cast<size_t>(w.bh / p.num_heads) * p.max_blocks + pos / p.page_size];
+      const int b = p.block_table[static_cast<size_t>(w.bh / p.num_heads) * p.max_blocks + pos / p.page_size];
+      // any other id outside the cache reads as zeros too; clamping it keeps
+      // block * heads + head inside int for the 5-D map
+      return static_cast<unsigned>(b) < static_cast<unsigned>(p.num_blocks) ? b : p.num_blocks;
     };
     // split mode: this warp draws the work tiles (the first one is the
     // CTA's index, each further one comes from the global counter once the
@@ -404,9 +422,15 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             if (lane < chunks) {
               const int head = tl.bh % p.num_heads;
               const int pos = key0 + lane * rows;
-              for (int h = 0; h < C::kHalves; ++h)
-                ptx::tma_load_4d(sKV(slot) + h * C::kHalfBytes + lane * rows * 128, map, done, h * 64,
-                                 pos % p.page_size, head, blk);
+              if constexpr (kPairedHalves) {
+                // 5-D map [block * heads + head][8-key group][half][key][64]
+                ptx::tma_load_5d(sKV(slot) + lane * rows * 256, map, done, 0, 0, 0,
+                                 (pos % p.page_size) / 8, blk * p.num_heads + head);
+              } else {
+                for (int h = 0; h < C::kHalves; ++h)
+                  ptx::tma_load_4d(sKV(slot) + h * C::kHalfBytes + lane * rows * 128, map, done, h * 64,
+                                   pos % p.page_size, head, blk);
+              }
             }
             __syncwarp();
             if (scrub) {
@@ -417,11 +441,12 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
               }
               ++scrubs;
               uint8_t* vt = smem + C::kOffKV + slot * C::kTileBytes;
-              const int n16 = (C::kBlockN - valid) * 8;  // 16-byte pieces per half
-              for (int i = lane; i < C::kHalves * n16; i += 32) {
-                const int h = i / n16, r = i - h * n16;
-                *reinterpret_cast<uint4*>(vt + h * C::kHalfBytes + valid * 128 + r * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
+              // 16-byte pieces of keys valid..127: 8 per key and half
+              constexpr int kPerKey = 8 * C::kHalves;
+              for (int i = lane; i < (C::kBlockN - valid) * kPerKey; i += 32) {
+                const int key = valid + i / kPerKey, r = i % kPerKey;
+                *reinterpret_cast<uint4*>(vt + (key / 8) * kKVGroupBytes + (r / 8) * kKVHalfBytes +
+                                          (key % 8) * 128 + (r % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
               }
               ptx::fence_proxy_async_smem();  // visible to the tensor core's reads
               __syncwarp();
@@ -500,12 +525,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       // its per-MMA work to an add and the instruction itself matters.
       // Every lane of the warp runs this loop with the same values; that
       // keeps them warp-uniform, and an elected lane issues.
-      // Q and K tiles: K-major, 128-byte swizzle, 8-row groups 1 KiB apart.
+      // Q and K tiles: K-major, 128-byte swizzle, 8-row groups (SBO) 1 KiB
+      // apart (K: kKVGroupBytes).
       const uint64_t dQ00 = ptx::desc_sw128(sQ(0, 0), 16, 1024);
-      const uint64_t dK0 = ptx::desc_sw128(sKV(0), 16, 1024);
-      // V tiles: MN-major (d contiguous), d-halves 16 KiB apart (LBO),
-      // 8-key groups 1 KiB apart (SBO).
-      const uint64_t dV0 = ptx::desc_sw128(sKV(0), C::kHalfBytes, 1024);
+      const uint64_t dK0 = ptx::desc_sw128(sKV(0), 16, kKVGroupBytes);
+      // V tiles: MN-major (d contiguous), d-halves kKVHalfBytes apart (LBO),
+      // 8-key groups kKVGroupBytes apart (SBO).
+      const uint64_t dV0 = ptx::desc_sw128(sKV(0), kKVHalfBytes, kKVGroupBytes);
       auto slot_off = [](int slot) -> uint64_t {
         return static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
       };
@@ -517,9 +543,11 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t koff =
+            const uint64_t qoff =
                 static_cast<uint64_t>(((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4);
-            ptx::mma_ss(ts, dq + koff, dk + koff, kIdescS, kk > 0 ? 1u : 0u);
+            const uint64_t koff =
+                static_cast<uint64_t>(((kk >> 2) * kKVHalfBytes + (kk & 3) * 32) >> 4);
+            ptx::mma_ss(ts, dq + qoff, dk + koff, kIdescS, kk > 0 ? 1u : 0u);
           }
         }
         __syncwarp();
@@ -533,7 +561,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         if (ptx::elect_one()) {
 #pragma unroll
           for (int kk = 0; kk < C::kBlockN / 16; ++kk)
-            ptx::mma_ts(to, ts + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+            ptx::mma_ts(to, ts + kk * 8, dv + static_cast<uint64_t>((kk * 2 * kKVGroupBytes) >> 4),
                         kIdescO, (!first || kk > 0) ? 1u : 0u);
         }
         __syncwarp();

@@ -77,6 +77,14 @@ int launch_merge(const float* o_part, const float* lse_part, void* o, float* lse
   mcfg.gridDim = dim3(static_cast<unsigned>(Nq), static_cast<unsigned>(BH), 1);
   mcfg.blockDim = dim3(static_cast<unsigned>(d), 1, 1);
   mcfg.stream = st;
+  // programmatic dependent launch: the merge grid is set up while the
+  // partial pass runs and starts on the SMs it leaves; the kernel waits for
+  // the partials before reading them
+  cudaLaunchAttribute attr[1] = {};
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  mcfg.attrs = attr;
+  mcfg.numAttrs = 1;
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(o);
   cudaError_t err;
   const int parts = kPartsPerSplit * splits;
@@ -157,6 +165,9 @@ int mha_fwd_paged(const void* q, const void* k_cache, const void* v_cache, const
   const long long BH = static_cast<long long>(B) * H;
   if (BH == 0 || Nq == 0) return MHA_OK;
   if (max_blocks == 0 || num_blocks == 0) return MHA_ERR_INVALID_ARG;
+  // the kernel addresses a page as block * H + head, in int, with block up
+  // to num_blocks (the id that reads as zeros)
+  if ((static_cast<long long>(num_blocks) + 1) * H > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
   if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !o || !lse || !workspace)
     return MHA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) ||

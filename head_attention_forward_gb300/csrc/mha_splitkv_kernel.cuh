@@ -16,6 +16,8 @@
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "sm103_ptx.cuh"
+
 namespace mha {
 
 constexpr int kSplitMaxQ = 16;  // queries per call (decode-sized blocks)
@@ -42,6 +44,9 @@ __global__ void __launch_bounds__(D) splitkv_merge_kernel(const float* o_part, c
   // Paged caches: an entry has only the partials of the splits that hold
   // some of its keys (the partial pass skips the others and leaves their
   // slots unwritten).
+  // launched as a programmatic dependent of the partial pass: its CTAs may
+  // be resident before that pass ends, so wait for its results here
+  ptx::griddep_wait();
   int ns = num_splits;
   if (seq_lens) {
     const long long nk = max(0, min(seq_lens[bh / num_heads], max_keys));

@@ -74,6 +74,27 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Tiled 5-D load; same completion rule as tma_load_3d.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int x, int y, int z, int w, int v) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "r"(z), "r"(w), "r"(v)
+      : "memory");
+}
+
+// Programmatic dependent launch.  launch_dependents: this CTA no longer
+// holds back the launch of the next kernel in the stream (the one launched
+// with programmatic stream serialisation); that grid starts once every CTA
+// of this one has signalled or exited.  dependency_wait: blocks until the
+// grid this one depends on has completed and its memory writes are visible
+// (returns at once for a normal launch).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Orders this thread's earlier generic-proxy shared-memory writes before
 // later async-proxy accesses (TMA copies, tcgen05.mma operand reads).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -117,6 +117,7 @@ int mha_fwd_kv(const void *q, const void *k, const void *v, void *o, float *lse,
  *                 t % page_size of block block_table[b][t / page_size].
  *   o, lse      : as for mha_fwd_kv.
  *   page_size   : 16, 32, 64, 128 or 256.
+ *   num_blocks  : >= 1, with (num_blocks + 1) * H <= INT_MAX.
  *   causal      : bottom-right aligned per batch entry (query i of entry b
  *                 sees keys 0 .. seq_lens[b]-Nq+i); a query with no visible
  *                 key gets O = 0, LSE = -inf.

@@ -143,6 +143,7 @@ def test_paged_argument_checks(L):
     assert call(page=512) == mha.MHA_ERR_INVALID_ARG
     assert call(mb=0) == mha.MHA_ERR_INVALID_ARG
     assert call(nb=0) == mha.MHA_ERR_INVALID_ARG
+    assert call(nb=1 << 30, H=2) == mha.MHA_ERR_INVALID_ARG   # block * H + head overflows int
     assert call(bt=0) == mha.MHA_ERR_INVALID_ARG
     assert call(bt=4 * big + 2) == mha.MHA_ERR_MISALIGNED
     assert call(d=80) == mha.MHA_ERR_UNSUPPORTED_DIM

@@ -197,6 +197,7 @@ def test_paged_odd_tables(page):
     table[0, 1] = table[0, 3]            # one physical block used twice
     table[1, 2] = num_blocks + 5         # past the cache
     table[1, 4] = -3                     # negative
+    table[2, 5] = 1 << 30                # far past the cache
     seq = np.array([max_blocks * page - 5, 5 * page + 7, max_blocks * page + 100], dtype=np.int32)
     kc = synth.normal_bf16(70 + page, synth.STREAM_K, num_blocks * H * page * d).reshape(num_blocks, H, page, d)
     vc = synth.normal_bf16(70 + page, synth.STREAM_V, num_blocks * H * page * d).reshape(num_blocks, H, page, d)

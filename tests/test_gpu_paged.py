@@ -41,9 +41,9 @@ def gather(kc, table, b, n, page):
     return np.ascontiguousarray(np.stack(rows, axis=1))
 
 
-@pytest.mark.parametrize("page", [16, 64, 128])
+@pytest.mark.parametrize("page", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
-@pytest.mark.parametrize("d,Nq", [(128, 1), (64, 4), (64, 2)])
+@pytest.mark.parametrize("d,Nq", [(128, 1), (128, 16), (64, 4), (64, 2)])
 def test_paged_against_oracle(page, causal, d, Nq):
     import torch
 

@@ -321,7 +321,7 @@ def run_decode(args, name):
                      "frac": gbs / hbm_peak, "traffic": recorded_traffic(name),
                      "algorithmic_bytes_per_step": algo_bytes,
                      "kernel": f"mha_fwd_kernel<{d},{int(bool(causal))},split> + splitkv_merge_kernel<{d}>"},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -396,7 +396,7 @@ def run_paged(args, name):
                      "peak_source": src, "traffic": recorded_traffic(name),
                      "algorithmic_bytes_per_step": algo_bytes,
                      "kernel": f"mha_fwd_kernel<{d},{int(bool(causal))},split,paged> + splitkv_merge_kernel<{d}>"},
-        "gpu_launches": 2 * args.steps, "clocks": clk.summary(),
+        "gpu_launches": 3 * args.steps, "clocks": clk.summary(),
     }), flush=True)
     return 0
 

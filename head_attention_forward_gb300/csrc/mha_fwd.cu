@@ -187,6 +187,16 @@ cudaError_t launch_split(int d, bool causal, const CUtensorMap& mq, const CUtens
 
 namespace mha_host {
 
+// Zeroes the split pass's work-tile counter with a one-thread kernel; the
+// split pass is launched next as its programmatic dependent.
+static cudaError_t reset_counter(int* counter, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(1, 1, 1);
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, mha::split_counter_reset_kernel, counter);
+}
+
 int fwd_split_partial(const void* q, const void* k, const void* v, float* o_part, float* lse_part,
                       int* tile_counter, int BH, int Nq, int Nk, int d, float scale, bool causal,
                       int num_splits, int tiles_per_split, int dev, unsigned* status, cudaStream_t st) {
@@ -208,7 +218,7 @@ int fwd_split_partial(const void* q, const void* k, const void* v, float* o_part
   prm.lse_part = lse_part;
   prm.tile_counter = tile_counter;
   prm.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  if (cudaMemsetAsync(tile_counter, 0, sizeof(int), st) != cudaSuccess) return MHA_ERR_CUDA;
+  if (reset_counter(tile_counter, st) != cudaSuccess) return MHA_ERR_CUDA;
   const cudaError_t err = launch_split<false>(d, causal, mq, mk, mv, prm, device_sms(dev), st);
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -245,7 +255,7 @@ int fwd_paged_partial(const void* q, const void* k_cache, const void* v_cache,
   prm.num_heads = H;
   prm.num_blocks = num_blocks;
   prm.tile_counter = tile_counter;
-  if (cudaMemsetAsync(tile_counter, 0, sizeof(int), st) != cudaSuccess) return MHA_ERR_CUDA;
+  if (reset_counter(tile_counter, st) != cudaSuccess) return MHA_ERR_CUDA;
   const cudaError_t err = launch_split<true>(d, causal, mq, mk, mv, prm, device_sms(dev), st);
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
@@ -268,6 +278,15 @@ cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[1] = {};
+  if (SPLIT) {
+    // a programmatic dependent of split_counter_reset_kernel, queued just
+    // before it (the kernel waits for that one before its first read)
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
   return cudaLaunchKernelEx(&cfg, mha::mha_fwd_kernel<D, CAUSAL, SPLIT, PAGED>, mq, mk, mv, prm);
 }
 

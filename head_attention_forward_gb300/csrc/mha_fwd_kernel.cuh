@@ -133,10 +133,19 @@ __device__ __forceinline__ int fwd_tile_of_round(int k, int c, int G) {
   return k * G + ((k & 1) ? (G - 1 - c) : c);
 }
 
+// Zeroes the split pass's work-tile counter before each call.  The split
+// pass is launched as its programmatic dependent, so that pass's CTAs set up
+// while this one-thread kernel runs.
+__global__ void split_counter_reset_kernel(int* counter) {
+  ptx::griddep_launch_dependents();
+  *counter = 0;
+}
+
 // SPLIT = false: the attention forward pass (square, top-left causal mask).
 // SPLIT = true: the partial pass of split-KV decoding (bottom-right causal
-// mask, fp32 partial outputs for splitkv_merge_kernel); only stage 0 is used,
-// the Q buffers of both stages serve as two Q sets, and work tiles are
+// mask, fp32 partial outputs for splitkv_merge_kernel); a split's K/V tiles
+// alternate between the two stages, each of which writes a partial of its
+// own, the Q buffers of both stages serve as two Q sets, and work tiles are
 // handed out at run time.
 // PAGED = true (with SPLIT): the same pass over a paged K/V cache, each
 // batch entry with its own key count; tmK / tmV then map the cache
@@ -309,8 +318,14 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // split mode: the merge kernel may start on SMs this grid leaves (it
-  // waits for this grid's completion before reading any partial)
-  if (SPLIT && threadIdx.x == 0) ptx::griddep_launch_dependents();
+  // waits for this grid's completion before reading any partial).  This
+  // grid is itself a dependent of split_counter_reset_kernel: the set-up
+  // above overlaps that kernel, and nothing below runs before it and all
+  // work queued ahead of it have completed.
+  if constexpr (SPLIT) {
+    if (threadIdx.x == 0) ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+  }
 
   if (warp == 0) {
     // -------------------------------------------------- K/V producer

@@ -91,8 +91,11 @@ int mha_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
  *             aligned, at least mha_fwd_kv_workspace_size(...) bytes, not
  *             overlapping any other argument.  Its contents need no
  *             initialisation and are garbage afterwards.
- *   stream  : cudaStream_t; a 4-byte memset (of a work-tile counter in
- *             the workspace) and two kernels are queued on it.
+ *   stream  : cudaStream_t; three kernels are queued on it: one that
+ *             zeroes a work-tile counter in the workspace, the partial pass
+ *             and the merge.  The last two are launched as programmatic
+ *             dependents of the kernel before them: each may start while
+ *             that one runs and waits for its results before reading them.
  *
  * B*H == 0 or Nq == 0 is a no-op.  Errors as for mha_fwd.
  */

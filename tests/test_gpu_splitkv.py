@@ -121,8 +121,8 @@ def test_splitkv_full_workload_sampled_heads(name):
 
 
 def test_splitkv_in_cuda_graph():
-    """The split-KV call captured in a CUDA graph (its counter memset and
-    both kernels) and replayed three times on a dirty workspace gives the
+    """The split-KV call captured in a CUDA graph (its counter reset and the
+    two dependent kernels) and replayed three times on a dirty workspace gives the
     result of a direct call, bit for bit, and the forward pass captured the
     same way matches its direct call too."""
     import torch

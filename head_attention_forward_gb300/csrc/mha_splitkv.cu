@@ -20,10 +20,22 @@ using namespace mha_host;
 // time.  Each work tile costs a pipeline drain at its end, so fewer, longer
 // ones do better until the last ones leave CTAs idle: about six per CTA
 // measured best on decode shapes (88-98% of the HBM copy rate against
-// 84-88% with 32 per CTA).  A fixed constant keeps the workspace size a
-// pure function of the problem shape.
+// 84-88% with 32 per CTA).
+//
+// Small problems (at most kOneWaveTiles K/V tiles per SM) are latency-bound
+// rather than bandwidth-bound: there at most one work tile per SM, with an
+// even number of K/V tiles (the two stages take alternate tiles), measured
+// 8-33% faster than six per SM (one query on 32 heads x 4k keys: 16.5 us
+// against 20.6; 8 heads x 16k keys: 17.5 against 26.1).  That needs fewer
+// heads than SMs, and a head count whose splits keep at least 4/5 of the
+// SMs busy.  At ~108 tiles per SM six per SM was still 1.4% ahead.
+//
+// Fixed constants (the SM count of a GB300) keep the workspace size a pure
+// function of the problem shape.
 constexpr int kTileKeys = 128;
-constexpr int kTargetTiles = 6 * 152;
+constexpr int kPlanSMs = 152;
+constexpr int kTargetTiles = 6 * kPlanSMs;
+constexpr int kOneWaveTiles = 64;
 
 struct Plan {
   int splits = 0, tiles_per_split = 0;
@@ -39,10 +51,15 @@ constexpr int kPartsPerSplit = 2;
 Plan make_plan(long long BH, int Nq, int Nk, int d, int num_splits) {
   Plan pl;
   const int tiles = (Nk + kTileKeys - 1) / kTileKeys;
+  const bool one_wave = num_splits == 0 && BH < kPlanSMs &&
+                        BH * tiles <= static_cast<long long>(kOneWaveTiles) * kPlanSMs &&
+                        5 * (kPlanSMs / BH) * BH >= 4 * kPlanSMs;
   int want = num_splits > 0 ? num_splits
+             : one_wave     ? static_cast<int>(kPlanSMs / BH)
                             : static_cast<int>(std::max<long long>(1, (kTargetTiles + BH - 1) / BH));
   want = std::max(1, std::min(want, tiles));
   pl.tiles_per_split = (tiles + want - 1) / want;
+  if (one_wave && pl.tiles_per_split > 1 && (pl.tiles_per_split & 1)) ++pl.tiles_per_split;
   pl.splits = (tiles + pl.tiles_per_split - 1) / pl.tiles_per_split;
   pl.o_part_bytes = static_cast<size_t>(BH) * kPartsPerSplit * pl.splits * Nq * d * 4;
   pl.lse_part_bytes = static_cast<size_t>(BH) * kPartsPerSplit * pl.splits * Nq * 4;

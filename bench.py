@@ -91,12 +91,16 @@ KERNEL_SOURCES = {
 
 
 def kernel_source_hash(kernel: str) -> str:
+    """Hash of the kernel's code: its source files with // comments, trailing
+    blanks and empty lines removed, so that editing a comment keeps the
+    recorded traffic of an unchanged kernel."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "head_attention_forward_gb300", "csrc")
     for fn in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+        with open(os.path.join(csrc, fn), encoding="utf-8") as f:
+            code = [ln.split("//", 1)[0].rstrip() for ln in f]
+        h.update(fn.encode() + "\n".join(ln for ln in code if ln).encode())
     return h.hexdigest()[:16]
 
 

@@ -46,8 +46,11 @@
 // each stage and the other softmax warps have no work; a split's K/V tiles
 // alternate between the stages, so the two stages' softmax warps work on
 // consecutive tiles at once; each stage writes an fp32 partial output and
-// its LSE for a merge kernel (two partials per split).  PAGED gathers each 128-key tile of a paged
-// K/V cache from page-sized TMA boxes named by a block table.
+// its LSE for a merge kernel (two partials per split).  The split pass runs
+// between two programmatic-dependent launches: after the kernel that zeroes
+// its work-tile counter, before the merge kernel.  PAGED gathers each
+// 128-key tile of a paged K/V cache from page-sized TMA boxes named by a
+// block table (at d = 128 one box holds both d-halves of its rows).
 //
 // Every mbarrier wait is bounded (clock64 budget).  A wait that runs out
 // records a code in the device status word, raises a CTA-wide abort flag

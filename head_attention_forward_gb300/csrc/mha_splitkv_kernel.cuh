@@ -27,7 +27,8 @@ constexpr int kSplitMaxQ = 16;  // queries per call (decode-sized blocks)
 // splits t, t + D, ...) and their weights staged in shared memory D at a
 // time, so the partial outputs' loads are independent and many are in
 // flight at once: a serial walk over the splits is one L2 round trip per
-// split.
+// split.  Up to 32 partials, the partial outputs are loaded together with
+// the LSEs, before the weights are known.
 template <int D>
 __global__ void __launch_bounds__(D) splitkv_merge_kernel(const float* o_part, const float* lse_part,
                                                          __nv_bfloat16* o, float* lse, int Nq,
@@ -54,9 +55,22 @@ __global__ void __launch_bounds__(D) splitkv_merge_kernel(const float* o_part, c
                               parts_per_split * ((nk + split_keys - 1) / split_keys)));
   }
   auto lse_of = [&](int s) { return lse_part[(base + s) * Nq + qi]; };
+  const float* src = o_part + (base * Nq + qi) * D + c;
+  const size_t stride = static_cast<size_t>(Nq) * D;
+  // Up to kMergeRegs partials (the usual case): every load, the LSEs and
+  // this thread's column of each partial output, is issued before the first
+  // result is used, so the merge costs one round trip to L2, not three.
+  constexpr int kMergeRegs = 32;
+  const bool in_regs = ns <= kMergeRegs;
+  float ov[kMergeRegs];
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < kMergeRegs; ++i) ov[i] = i < ns ? src[i * stride] : 0.f;
+  }
   // the largest split LSE
-  float m = -INFINITY;
-  for (int s = c; s < ns; s += D) m = fmaxf(m, lse_of(s));
+  const float my_lse = c < ns ? lse_of(c) : -INFINITY;
+  float m = my_lse;
+  for (int s = c + D; s < ns; s += D) m = fmaxf(m, lse_of(s));
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
   if (lane == 0) red[warp] = m;
@@ -67,18 +81,29 @@ __global__ void __launch_bounds__(D) splitkv_merge_kernel(const float* o_part, c
   float out = 0.f, lse_row = -INFINITY;
   if (lmax != -INFINITY) {  // uniform across the block
     float wsum = 0.f, acc = 0.f;
-    for (int s0 = 0; s0 < ns; s0 += D) {
-      const int n = min(D, ns - s0);
-      __syncthreads();  // the previous chunk's weights are no longer read
-      if (c < n) w_s[c] = __expf(lse_of(s0 + c) - lmax);
+    if (in_regs) {
+      if (c < ns) w_s[c] = __expf(my_lse - lmax);
       __syncthreads();
-      const float* src = o_part + ((base + s0) * Nq + qi) * D + c;
-      const size_t stride = static_cast<size_t>(Nq) * D;
+#pragma unroll
+      for (int i = 0; i < kMergeRegs; ++i) {
+        if (i < ns) {
+          const float w = w_s[i];
+          wsum += w;
+          acc = fmaf(w, ov[i], acc);
+        }
+      }
+    } else {
+      for (int s0 = 0; s0 < ns; s0 += D) {
+        const int n = min(D, ns - s0);
+        __syncthreads();  // the previous chunk's weights are no longer read
+        if (c < n) w_s[c] = __expf((s0 == 0 ? my_lse : lse_of(s0 + c)) - lmax);
+        __syncthreads();
 #pragma unroll 8
-      for (int i = 0; i < n; ++i) {
-        const float w = w_s[i];
-        wsum += w;
-        acc = fmaf(w, src[i * stride], acc);
+        for (int i = 0; i < n; ++i) {
+          const float w = w_s[i];
+          wsum += w;
+          acc = fmaf(w, src[(s0 + i) * stride], acc);
+        }
       }
     }
     out = acc / wsum;

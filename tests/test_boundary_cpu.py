@@ -102,6 +102,38 @@ def test_kv_workspace_size_is_pure():
     assert mha.mha_fwd_kv_workspace_size(0, 1, 1, 100, 64, 0) == 0    # empty
 
 
+def _kv_workspace(B, H, Nq, Nk, d, splits):
+    """Workspace bytes for a given split count: o_part fp32 [B*H, 2*splits,
+    Nq, d], lse_part fp32 [B*H, 2*splits, Nq] (16-byte aligned), then the
+    16-byte counter slot."""
+    o = B * H * 2 * splits * Nq * d * 4
+    lse = B * H * 2 * splits * Nq * 4
+    return (o + 15) // 16 * 16 + (lse + 15) // 16 * 16 + 16
+
+
+@pytest.mark.parametrize("shape,splits", [
+    # one wave: fewer heads than the 152 SMs, at most 64 K/V tiles per SM and
+    # splits filling >= 4/5 of the SMs; floor(152 / (B*H)) splits, rounded so
+    # that each split has an even number of 128-key tiles
+    ((1, 32, 1, 4096, 128), 4),     # 32 tiles: 4 splits of 8
+    ((1, 8, 1, 16384, 128), 16),    # 19 splits would be 7 tiles each: 8 -> 16 splits
+    ((4, 8, 4, 8192, 64), 4),
+    ((1, 16, 1, 32768, 128), 9),    # 256 tiles: 9 splits of 30 (29 rounded up)
+    ((1, 151, 1, 8192, 128), 1),
+    ((1, 1, 1, 300, 128), 3),       # 3 tiles: one per split
+    # six work tiles per SM: ceil(912 / (B*H)) splits
+    ((4, 32, 1, 16384, 128), 8),    # ~108 tiles per SM
+    ((1, 100, 1, 4096, 128), 8),    # 100 heads leave a third of the SMs idle in one wave
+    ((8, 32, 1, 32768, 128), 4),    # 256 heads: more heads than SMs
+    ((1, 32, 4, 131072, 128), 29),  # 1024 tiles per head, ~216 per SM
+])
+def test_kv_split_plan(shape, splits):
+    """The automatic split count, seen through the workspace size."""
+    import head_attention_forward_gb300 as mha
+    assert mha.mha_fwd_kv_workspace_size(*shape, 0) == _kv_workspace(*shape, splits)
+    assert mha.mha_fwd_kv_workspace_size(*shape, splits) == _kv_workspace(*shape, splits)
+
+
 def test_kv_argument_checks(L):
     import head_attention_forward_gb300 as mha
     big = 1 << 40

@@ -61,3 +61,57 @@ def assert_close(o_gpu, lse_gpu, o_ref, lse_ref, what: str = ""):
     assert do.mean() <= TOL_MEAN_O, msg
     assert dl.max() <= TOL_MAX_LSE, msg
     return do.max(), do.mean(), dl.max()
+
+
+# Parity figures of the whole-tensor comparisons, printed at the end of the
+# session (tests/conftest.py) so that a quiet run still shows them.
+PARITY_STATS: list[tuple[str, float, float, float]] = []
+
+
+def _source_digest() -> str:
+    """Digest of the oracle's and the input generator's sources: a cached
+    oracle output is reused only while both are unchanged."""
+    import hashlib
+    import os
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    h = hashlib.sha256()
+    for rel in ("oracle/mha_oracle.c", "oracle/__init__.py", "synth/__init__.py", "synth/synth_gen.c"):
+        with open(os.path.join(root, rel), "rb") as f:
+            h.update(rel.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def oracle_fwd_cached(name: str, q, k, v, scale: float, causal: bool):
+    """The oracle's O and LSE for a named workload, cached on disk by
+    (workload, seed, shape, sources of the oracle and the generator).
+
+    The cache only saves the oracle's minute on a rerun; every value in it
+    was written by oracle.attention_fwd.  Directory: $MHA_ORACLE_CACHE, else
+    ~/.cache/mha_fwd_oracle.
+    """
+    import os
+
+    import oracle
+    c = synth.CONFIGS[name]
+    key = (f"{name}-s{c['seed']}-{'x'.join(map(str, q.shape))}-c{int(bool(causal))}"
+           f"-{np.float32(scale).view(np.uint32):08x}-{_source_digest()}")
+    root = os.environ.get("MHA_ORACLE_CACHE", os.path.join(os.path.expanduser("~"), ".cache", "mha_fwd_oracle"))
+    po, pl = os.path.join(root, key + ".o.npy"), os.path.join(root, key + ".lse.npy")
+    if os.path.exists(po) and os.path.exists(pl):
+        try:
+            o, lse = np.load(po), np.load(pl)
+            if o.shape == q.shape and lse.shape == q.shape[:3]:
+                return o, lse
+        except (OSError, ValueError):
+            pass
+    o, lse = oracle.attention_fwd(q, k, v, scale, causal)
+    try:
+        os.makedirs(root, exist_ok=True)
+        for path, arr in ((po, o), (pl, lse)):
+            tmp = f"{path}.{os.getpid()}.tmp"
+            with open(tmp, "wb") as f:
+                np.save(f, arr)
+            os.replace(tmp, path)
+    except OSError:
+        pass  # an unwritable cache only costs the next run the oracle's time
+    return o, lse

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "mha_fwd.h"
+#include "mha_internal.h"
 
 namespace {
 
@@ -29,14 +30,22 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch buffer on the current device, looked up
-// once per device (with that device current) and cached.
+// once per device (with that device current) and cached.  The library's
+// device check runs first, so a GPU the kernels cannot run on is reported
+// as MHA_ERR_NO_DEVICE, as mha_fwd_kv reports it, before any lookup.
 int scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MHA_ERR_NO_DEVICE;
+  unsigned* status = nullptr;
+  const int rc = mha_host::device_setup(&dev, &status);
+  if (rc != MHA_OK) return rc;
+  if (dev >= kMaxDevices) return MHA_ERR_NO_DEVICE;
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_kv_scratch) != cudaSuccess || p == nullptr) return MHA_ERR_CUDA;
+    if (cudaGetSymbolAddress(&p, g_kv_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();  // leave no pending error behind for the caller
+      return MHA_ERR_CUDA;
+    }
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
@@ -56,7 +65,9 @@ extern "C" int mha_fwd_kv_noalloc(const void* q, const void* k, const void* v, v
   const int rc = scratch_address(&scratch);
   if (rc != MHA_OK) return rc;
   // Every element of the scratch that the merge step reads is written by the
-  // partial step of the same call, so nothing needs clearing between calls.
+  // partial step of the same call (when every device-side wait completes),
+  // and the work-tile counter is zeroed by the call's first kernel, so
+  // nothing needs clearing between calls.
   return mha_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, num_splits, scratch,
                     kScratchBytes, stream);
 }

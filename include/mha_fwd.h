@@ -24,6 +24,10 @@
  *     device memory; it keeps one status word per device in module memory.
  *   - No call throws, aborts or exits.  A non-zero return means nothing
  *     useful was written to the outputs.
+ *   - Per-device set-up (the architecture check, kernel attributes and the
+ *     status word's address) happens on the first call on each device and
+ *     is cached.  cudaDeviceReset discards the module memory that cache
+ *     points into: do not call the library on a device after resetting it.
  */
 #ifndef MHA_FWD_H
 #define MHA_FWD_H
@@ -165,6 +169,12 @@ size_t mha_fwd_kv_workspace_size(int B, int H, int Nq, int Nk, int d, int num_sp
  *     element a call reads back was written earlier in the same call.  Calls
  *     whose execution overlaps on the GPU (for example on two streams) race
  *     on the buffer and must be serialised by the caller.
+ *   - If mha_device_status reports MHA_ERR_TIMEOUT after a call, that call's
+ *     o and lse are undefined: a work tile that gave up may have left its
+ *     part of the buffer holding an earlier call's data.
+ *   - The buffer's device address is cached per device.  After
+ *     cudaDeviceReset the library's module memory is gone; the library must
+ *     not be called again on that device in the same process.
  */
 int mha_fwd_kv_noalloc(const void *q, const void *k, const void *v, void *o, float *lse,
                        int B, int H, int Nq, int Nk, int d, float scale, int causal,

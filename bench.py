@@ -40,9 +40,15 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
-# NVIDIA's dense bf16 figure for one GB300 (without 2:4 sparsity), reported
-# beside the measured denominators
+# NVIDIA's dense bf16 figure for one GB300, reported beside the measured
+# denominators: the HGX B300 datasheet gives 36 PFLOP/s FP16/BF16 for eight
+# GPUs with 2:4 sparsity, i.e. 4.5 per GPU sparse and 2.25 dense.
 NOMINAL_BF16_TFLOPS = 2250.0
+# A timed region shorter than this runs before the board's power cap settles
+# the clock, the situation of the burst cuBLAS measurement; longer regions
+# are compared with the sustained one.
+BURST_REGION_S = 1.0
+L2_BYTES = 129e6
 METRIC = "attention fwd TFLOP/s and % of GB300 bf16 tensor peak, per (B,H,N,d,causal)"
 UNIT = "TFLOP/s"
 FALLBACK_PEAK_TFLOPS = 1900.0  # used only when MEASURED_PEAKS.json is absent
@@ -67,20 +73,25 @@ def host_cores() -> int:
 
 
 def load_peaks():
-    """(sustained, burst, source) dense bf16 peaks in TFLOP/s.
-
-    The timed region is hundreds of back-to-back launches (most of a second
-    under the board power cap), the situation of the sustained cuBLAS
-    measurement, so the roofline fraction uses the sustained figure; the
-    burst fraction is reported beside it."""
+    """(sustained, burst, source) dense bf16 peaks in TFLOP/s."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
             pk = json.load(f)
         burst = float(pk["bf16_tflops"])
         sustained = float(pk.get("bf16_tflops_sustained", burst))
-        return sustained, burst, "measured (MEASURED_PEAKS.json: bf16_tflops_sustained; burst beside it)"
+        return sustained, burst, "measured (MEASURED_PEAKS.json)"
     return FALLBACK_PEAK_SUSTAINED, FALLBACK_PEAK_TFLOPS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def pick_peak(region_s: float):
+    """The roofline denominator for a timed region of `region_s` seconds:
+    the burst cuBLAS figure below BURST_REGION_S (the clock has not yet
+    settled under the power cap), the sustained one above it."""
+    sustained, burst, src = load_peaks()
+    if region_s < BURST_REGION_S:
+        return burst, f"{src} bf16_tflops (burst: timed region {region_s:.3f} s < {BURST_REGION_S:.0f} s)"
+    return sustained, f"{src} bf16_tflops_sustained (timed region {region_s:.3f} s >= {BURST_REGION_S:.0f} s)"
 
 
 # Source files each kernel is compiled from; a recorded ncu traffic figure is
@@ -181,6 +192,112 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+class NvmlSampler:
+    """Reads the SM clock and the clock-event reasons in-process through
+    NVML, every `period_s`, on a thread of its own.  Only read-only queries
+    are made (clock info and event reasons); nothing is set.
+
+    Samples carry host timestamps, so a caller can keep those that fall
+    inside its timed region (`mark()` before and after it)."""
+
+    # nvmlClocksEventReason* bits of the reasons named in the timing rules
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.0005):
+        self.device_index = device_index
+        self.period_s = period_s
+        self.samples = []  # (host time, sm MHz, reasons bitmask)
+        self.marks = []
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._lib = None
+        self._h = None
+
+    def _open(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+        except OSError:
+            return False
+        if lib.nvmlInit_v2() != 0:
+            return False
+        h = ctypes.c_void_p()
+        bus = None
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(self.device_index)
+            bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        except Exception:
+            bus = None
+        ok = bus is not None and lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(self.device_index, ctypes.byref(h)) != 0:
+            return False
+        self._lib, self._h = lib, h
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        try:
+            self._reasons = lib.nvmlDeviceGetCurrentClocksEventReasons
+        except AttributeError:
+            self._reasons = lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return True
+
+    def _run(self):
+        import ctypes
+        mhz, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.perf_counter()
+            if self._lib.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(mhz)) == 0:
+                r = rs.value if self._reasons(self._h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((t, float(mhz.value), int(r)))
+            self._stop.wait(self.period_s)
+
+    def __enter__(self):
+        if self._open():
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+        if self._lib is not None:
+            self._lib.nvmlShutdown()
+
+    def mark(self):
+        self.marks.append(time.perf_counter())
+
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and the union of reasons over the samples taken
+        between t0 and t1 (default: the first two marks)."""
+        if t0 is None and len(self.marks) >= 2:
+            t0, t1 = self.marks[0], self.marks[1]
+        inside = [s for s in self.samples if (t0 is None or t0 <= s[0] <= t1)]
+        if not inside:
+            return None
+        reasons = sorted({nm for _, _, r in inside for bit, nm in self.REASON_BITS.items() if r & bit})
+        mhz = [m for _, m, _ in inside]
+        return {"sm_mhz": statistics.median(mhz), "sm_mhz_min": min(mhz), "sm_mhz_max": max(mhz),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(inside),
+                "source": f"NVML in-process, every {self.period_s * 1e3:.1f} ms"}
+
+
+def merge_clocks(nvml_summary, smi_summary):
+    """The clock record of a timed region: the in-process NVML samples inside
+    it, with the reasons nvidia-smi saw added (its 100 ms samples are too
+    coarse for the clock of a short region, but catch every reason)."""
+    if nvml_summary is None:
+        return smi_summary
+    out = dict(nvml_summary)
+    if smi_summary:
+        out["reasons"] = sorted(set(out["reasons"]) | set(smi_summary.get("reasons", [])))
+        out["nvidia_smi"] = smi_summary
+    return out
+
+
 def oracle_sample(c, q, k, v, rows_per_head: int, heads, nthreads: int = 0):
     """Times the oracle on `rows_per_head` evenly spread rows of each head in
     `heads`; returns (seconds, counted FLOPs of those rows, rows)."""
@@ -196,15 +313,27 @@ def oracle_sample(c, q, k, v, rows_per_head: int, heads, nthreads: int = 0):
     return dt, per_row * rows.size * len(heads), rows.size * len(heads)
 
 
-def size_oracle_sample(c, q, k, v, target_s: float):
+def size_oracle_sample(c, q, k, v, target_s: float, nthreads: int = 0):
     """(rows per head, number of heads) so that the oracle runs about target_s."""
     import oracle
     oracle.build()
-    dt, _, n = oracle_sample(c, q, k, v, 64, [0])
+    dt, _, n = oracle_sample(c, q, k, v, 64, [0], nthreads)
     per_row = max(dt / max(n, 1), 1e-6)
     rows = int(min(c["N"], max(16, target_s / per_row)))
     heads = int(max(1, min(c["B"] * c["H"], round(target_s / (per_row * rows)))))
     return rows, heads
+
+
+def config_dict(name, c, world: int = 1):
+    """The `config` object of a forward workload's JSON line (the same for
+    both arms, so that their lines name one workload)."""
+    set_bytes = 4 * c["B"] * c["H"] * c["N"] * c["d"] * 2
+    return {"workload": workload_name(name, c), "B": c["B"], "H": c["H"], "N": c["N"], "d": c["d"],
+            "causal": c["causal"], "seed": c["seed"], "sigma_qk": c["sigma_qk"], "sigma_v": c["sigma_v"],
+            "flops_per_step": counted_flops(c),
+            "l2": ("inputs larger than L2 (Q+K+V+O = %.0f MB > 129 MB)" % (set_bytes / 1e6)
+                   if set_bytes > L2_BYTES else "inputs fit L2; rotated over copies or L2 flushed"),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def run_reference(args, c, name):
@@ -216,23 +345,23 @@ def run_reference(args, c, name):
     import oracle
     q, k, v = synth.qkv(c["seed"], c["B"], c["H"], c["N"], c["d"], c["sigma_qk"], c["sigma_v"])
     budget = 150.0 / max(1, args.steps + args.warmup)
-    rows, _ = size_oracle_sample(c, q, k, v, budget)
+    cores = host_cores()
+    rows, _ = size_oracle_sample(c, q, k, v, budget, cores)
     for i in range(args.warmup):
-        oracle_sample(c, q, k, v, rows, [i % (c["B"] * c["H"])])
+        oracle_sample(c, q, k, v, rows, [i % (c["B"] * c["H"])], cores)
     tot_t, tot_f, tot_rows = 0.0, 0.0, 0
     for i in range(args.steps):
-        dt, fl, nr = oracle_sample(c, q, k, v, rows, [(i + args.warmup) % (c["B"] * c["H"])])
+        dt, fl, nr = oracle_sample(c, q, k, v, rows, [(i + args.warmup) % (c["B"] * c["H"])], cores)
         tot_t += dt
         tot_f += fl
         tot_rows += nr
     value = tot_f / tot_t / 1e12
-    cores = oracle.num_threads()
     sample = f"{rows} evenly spaced query rows of one head per step ({tot_rows} rows total)"
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": workload_name(name, c)},
+        "data": "synthetic", "config": config_dict(name, c, 1),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -404,6 +533,96 @@ def run_paged(args, name):
     }), flush=True)
     return 0
 
+_INPUT_CACHE = {}
+
+
+def time_forward_config(mha, name, dev, stream, min_steps: int, min_region_s: float = 0.2):
+    """One forward workload timed on its own, for the per_config block.
+
+    Inputs larger than L2 run back to back.  Smaller ones rotate over enough
+    copies of Q, K, V, O and LSE that each launch finds its inputs evicted
+    (more than twice L2 in all); where that would take more than 16 copies
+    (the tiny workload), L2 is flushed before every launch instead and each
+    launch is timed alone.  At least `min_steps` launches, and enough for
+    about `min_region_s` seconds, so that the in-process clock samples cover
+    the region."""
+    import torch
+    c = synth.CONFIGS[name]
+    B, H, N, d, causal = c["B"], c["H"], c["N"], c["d"], c["causal"]
+    key = (c["seed"], B, H, N, d, c["sigma_qk"], c["sigma_v"])
+    if key not in _INPUT_CACHE:
+        _INPUT_CACHE.clear()
+        _INPUT_CACHE[key] = synth.config_inputs(name)
+    qb, kb, vb = _INPUT_CACHE[key]
+    set_bytes = 4 * qb.nbytes + 4 * B * H * N
+    copies = 1 if set_bytes > L2_BYTES else int(math.ceil(2 * L2_BYTES / set_bytes))
+    flush = None
+    if copies > 16:
+        copies = 1
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    def dev_tensor(bits):
+        return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(dev)
+    q0, k0, v0 = dev_tensor(qb), dev_tensor(kb), dev_tensor(vb)
+    sets = []
+    for i in range(copies):
+        q, k, v = (q0, k0, v0) if i == 0 else (q0.clone(), k0.clone(), v0.clone())
+        sets.append((q, k, v, torch.empty_like(q), torch.empty((B, H, N), dtype=torch.float32, device=dev)))
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    sptr = int(stream.cuda_stream)
+
+    def launch(i):
+        q, k, v, o, lse = sets[i % copies]
+        mha.mha_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, sptr)
+
+    for i in range(3):
+        launch(i)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(4):
+        launch(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    est_ms = max(e0.elapsed_time(e1) / 4, 1e-3)
+    steps = max(min_steps, int(math.ceil(min_region_s * 1e3 / est_ms)))
+    if flush is not None:
+        steps = min(steps, 400)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+    with NvmlSampler(dev.index) as nv:
+        torch.cuda.synchronize(dev)
+        nv.mark()
+        for i in range(steps):
+            if flush is not None:
+                flush.fill_(i & 255)
+            evs[2 * i].record(stream)
+            launch(i)
+            evs[2 * i + 1].record(stream)
+        torch.cuda.synchronize(dev)
+        nv.mark()
+    rc, word = mha.mha_device_status(sptr)
+    if rc != mha.MHA_OK:
+        raise RuntimeError(f"{name}: device status {rc} ({word:#x})")
+    per = [evs[2 * i].elapsed_time(evs[2 * i + 1]) for i in range(steps)]
+    if flush is None:
+        ms = evs[0].elapsed_time(evs[-1]) / steps  # back to back: launch gaps count
+        timing = ("back to back, inputs larger than L2" if copies == 1 else
+                  f"back to back, rotating over {copies} copies of the inputs ({copies * set_bytes / 1e6:.0f} MB)")
+    else:
+        ms = statistics.mean(per)
+        timing = "one launch at a time, each after a 256 MB write that flushes L2"
+    region_s = (nv.marks[1] - nv.marks[0]) if len(nv.marks) >= 2 else ms * steps / 1e3
+    peak, peak_src = pick_peak(region_s)
+    _, peak_burst, _ = load_peaks()
+    tf = counted_flops(c) / (ms / 1e3) / 1e12
+    clocks = nv.summary()
+    del sets, q0, k0, v0, flush
+    return {"workload": workload_name(name, c), "tflops": tf, "pct_of_peak": 100.0 * tf / peak,
+            "peak": peak, "peak_source": peak_src, "pct_of_burst_peak": 100.0 * tf / peak_burst,
+            "ms_per_launch": ms, "median_launch_ms": statistics.median(per), "steps": steps,
+            "timing": timing, "clocks": clocks,
+            "kernel": f"mha_fwd_kernel<{d},{'true' if causal else 'false'}>"}
+
+
 BWD_METRIC = ("attention bwd TFLOP/s (counted 10*B*H*N^2*d, halved when causal) and % of GB300 "
               "bf16 tensor peak, per (B,H,N,d,causal)")
 
@@ -494,6 +713,8 @@ def main():
                     + sorted(synth.PAGED_CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the chosen workload (no per_config block)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--backward", action="store_true",
                     help="time mha_bwd on the chosen forward workload instead of mha_fwd")
@@ -558,15 +779,17 @@ def main():
 
     # timed region: K launches, one event pair around each on the launch stream
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    with ClockSampler(dev.index) as clk:
+    with ClockSampler(dev.index) as clk, NvmlSampler(dev.index) as nv:
         if dist is not None:
             dist.barrier()
         torch.cuda.synchronize(dev)
+        nv.mark()
         evs[0].record(stream)
         for i in range(args.steps):
             step()
             evs[i + 1].record(stream)
         torch.cuda.synchronize(dev)
+        nv.mark()
         if dist is not None:
             dist.barrier()
     per_launch_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
@@ -596,7 +819,20 @@ def main():
     value = flops * args.steps * world / (total_ms / 1e3) / 1e12
     mean_launch_ms = statistics.mean(per_launch_ms)
     achieved = flops / (mean_launch_ms / 1e3) / 1e12
-    peak, peak_burst, peak_src = load_peaks()
+    peak_sustained, peak_burst, _ = load_peaks()
+    peak, peak_src = pick_peak(total_ms / 1e3)
+    clocks = merge_clocks(nv.summary(), clk.summary())
+    if clocks and clocks.get("sm_mhz"):
+        # launch duration in SM cycles at the median clock of the region,
+        # comparable with the cycles a profiler reports for one launch
+        clocks["cycles_per_launch"] = mean_launch_ms * 1e-3 * clocks["sm_mhz"] * 1e6
+
+    per_config = None
+    if world == 1 and not args.no_per_config:
+        per_config = {}
+        for other in synth.CONFIGS:
+            if other != name:
+                per_config[other] = time_forward_config(mha, other, dev, stream, args.steps)
 
     # End to end through the public C ABI: every step copies its Q, K, V from
     # pinned host memory to the device, runs mha_fwd, and copies O and LSE
@@ -664,10 +900,10 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
-        rows, heads = size_oracle_sample(c, qb, kb, vb, 15.0)
-        dt, fl, nr = oracle_sample(c, qb, kb, vb, rows, list(range(heads)))
-        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+        cores = host_cores()
+        rows, heads = size_oracle_sample(c, qb, kb, vb, 15.0, cores)
+        dt, fl, nr = oracle_sample(c, qb, kb, vb, rows, list(range(heads)), cores)
+        cpu = {"value": fl / dt / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{rows} evenly spaced query rows of each of heads 0..{heads - 1} "
                          f"({nr} rows, FLOPs counted as the metric counts them), fp64, {dt:.1f} s"}
 
@@ -676,14 +912,12 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_name(name, c), "B": B, "H": H, "N": N, "d": d,
-                       "causal": causal, "seed": c["seed"], "flops_per_step": flops,
-                       "l2": "inputs larger than L2 (Q+K+V+O = %.0f MB > 129 MB)"
-                             % (4 * qb.nbytes / 1e6) if 4 * qb.nbytes > 129e6 else "no flush; inputs fit L2",
-                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "config": config_dict(name, c, world),
             "pct_of_peak": 100.0 * value / world / peak,
             "pct_of_burst_peak": 100.0 * value / world / peak_burst,
+            "pct_of_sustained_peak": 100.0 * value / world / peak_sustained,
             "pct_of_nominal_peak": 100.0 * value / world / NOMINAL_BF16_TFLOPS,
+            "timed_region_s": total_ms / 1e3,
             "median_launch_ms": statistics.median(per_launch_ms),
             "cold_launch_ms": statistics.median(cold_ms),  # after an L2 flush
             # exponentials the softmax evaluates per second (one per visible
@@ -692,7 +926,9 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
                          "frac": achieved / peak, "peak_source": peak_src,
                          "peak_burst": peak_burst, "frac_burst": achieved / peak_burst,
+                         "peak_sustained": peak_sustained, "frac_sustained": achieved / peak_sustained,
                          "traffic": recorded_traffic(name),
+                         "algorithmic_flops_per_launch": flops,
                          "kernel": f"mha_fwd_kernel<{d},{'true' if causal else 'false'}>"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
@@ -700,9 +936,11 @@ def main():
                                  "download overlap step k's kernel",
                     "serial_value": serial_value},
             "gpu_launches": args.steps,
-            "clocks": clk.summary(),
+            "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if per_config is not None:
+            line["per_config"] = per_config
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -76,18 +76,20 @@ int device_setup(int* dev_out, unsigned** status_out) {
       fail |= cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
               cudaSuccess;
     };
-    smem_attr(mha::mha_fwd_kernel<64, false, false>, mha::FwdCfg<64>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<64, true, false>, mha::FwdCfg<64>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<128, false, false>, mha::FwdCfg<128>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<128, true, false>, mha::FwdCfg<128>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<64, false, true>, mha::FwdCfg<64>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<64, true, true>, mha::FwdCfg<64>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<128, false, true>, mha::FwdCfg<128>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<128, true, true>, mha::FwdCfg<128>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<64, false, true, true>, mha::FwdCfg<64>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<64, true, true, true>, mha::FwdCfg<64>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<128, false, true, true>, mha::FwdCfg<128>::kSmemBytes);
-    smem_attr(mha::mha_fwd_kernel<128, true, true, true>, mha::FwdCfg<128>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, false, false>, mha::FwdCfg<64, false>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, true, false>, mha::FwdCfg<64, false>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, false, false>, mha::FwdCfg<128, false>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, true, false>, mha::FwdCfg<128, false>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, false, false, false, true>, mha::FwdCfg<128, false>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, true, false, false, true>, mha::FwdCfg<128, false>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, false, true>, mha::FwdCfg<64, true>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, true, true>, mha::FwdCfg<64, true>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, false, true>, mha::FwdCfg<128, true>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, true, true>, mha::FwdCfg<128, true>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, false, true, true>, mha::FwdCfg<64, true>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<64, true, true, true>, mha::FwdCfg<64, true>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, false, true, true>, mha::FwdCfg<128, true>::kSmemBytes);
+    smem_attr(mha::mha_fwd_kernel<128, true, true, true>, mha::FwdCfg<128, true>::kSmemBytes);
     void* sym = nullptr;
     fail |= cudaGetSymbolAddress(&sym, g_status) != cudaSuccess;
     fail |= cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -170,18 +172,18 @@ long long wait_limit() {
 }  // namespace mha_host
 
 namespace {
-template <int D, bool CAUSAL, bool SPLIT, bool PAGED>
+template <int D, bool CAUSAL, bool SPLIT = false, bool PAGED = false, bool HMAJOR = false>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                   const mha::FwdParams& prm, int sms, cudaStream_t stream);
+                   const CUtensorMap& mo, const mha::FwdParams& prm, int sms, cudaStream_t stream);
 
 template <bool PAGED>
 cudaError_t launch_split(int d, bool causal, const CUtensorMap& mq, const CUtensorMap& mk,
                          const CUtensorMap& mv, const mha::FwdParams& prm, int sms, cudaStream_t st) {
   if (d == 64)
-    return causal ? launch<64, true, true, PAGED>(mq, mk, mv, prm, sms, st)
-                  : launch<64, false, true, PAGED>(mq, mk, mv, prm, sms, st);
-  return causal ? launch<128, true, true, PAGED>(mq, mk, mv, prm, sms, st)
-                : launch<128, false, true, PAGED>(mq, mk, mv, prm, sms, st);
+    return causal ? launch<64, true, true, PAGED>(mq, mk, mv, mq, prm, sms, st)
+                  : launch<64, false, true, PAGED>(mq, mk, mv, mq, prm, sms, st);
+  return causal ? launch<128, true, true, PAGED>(mq, mk, mv, mq, prm, sms, st)
+                : launch<128, false, true, PAGED>(mq, mk, mv, mq, prm, sms, st);
 }
 }  // namespace
 
@@ -265,16 +267,38 @@ int fwd_paged_partial(const void* q, const void* k_cache, const void* v_cache,
 namespace {
 using namespace mha_host;
 
+// The head-major order (m-blocks of one head adjacent; causal: pairs of
+// m-blocks of equal total cost, one pair per CTA per round) keeps the K/V of
+// the few heads in flight in L2.  It is used at d = 128 once all heads' K/V
+// no longer fit in L2, unless its rounds of equal work items would leave
+// more than 5% of the grid idle: the other order's snake rounds balance
+// unequal tiles better (at 2 x 32 heads x 4096 keys, causal, 512 pairs on
+// 152 SMs fill 84% of the last round's slots and measured 4% slower).
+bool use_head_major(int BH, int N, int d, bool causal, int sms) {
+  const double kv_bytes = 2.0 * BH * static_cast<double>(N) * d * 2.0;
+  if (d != 128 || kv_bytes <= 96.0 * (1 << 20)) return false;
+  const long long mblocks = (N + 255) / 256;
+  const long long items = static_cast<long long>(BH) * (causal ? (mblocks + 1) / 2 : mblocks);
+  const long long grid = items < sms ? items : sms;
+  const long long rounds = (items + grid - 1) / grid;
+  return static_cast<double>(items) >= 0.95 * static_cast<double>(rounds * grid);
+}
+
 // Persistent launch: one CTA per SM (fewer when there are fewer work tiles),
 // each walking its share of the (bh, m-block) or (bh, split) tiles.
-template <int D, bool CAUSAL, bool SPLIT = false, bool PAGED = false>
+// `mo` is used by the d = 128 square pass only (the others store O with
+// plain stores); callers of the other passes pass any map there.
+template <int D, bool CAUSAL, bool SPLIT, bool PAGED, bool HMAJOR>
 cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                   const mha::FwdParams& prm, int sms, cudaStream_t stream) {
+                   const CUtensorMap& mo, const mha::FwdParams& prm, int sms, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
-  const long long total = static_cast<long long>(prm.BH) * (SPLIT ? prm.num_splits : prm.num_mblocks);
+  // work tiles, or for the head-major order work items (causal: pairs of m-blocks)
+  const long long total =
+      static_cast<long long>(prm.BH) *
+      (SPLIT ? prm.num_splits : (HMAJOR && CAUSAL ? (prm.num_mblocks + 1) / 2 : prm.num_mblocks));
   cfg.gridDim = dim3(static_cast<unsigned>(total < sms ? total : sms), 1, 1);
-  cfg.blockDim = dim3(mha::FwdCfg<D>::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = mha::FwdCfg<D>::kSmemBytes;
+  cfg.blockDim = dim3(mha::FwdCfg<D, SPLIT>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = mha::FwdCfg<D, SPLIT>::kSmemBytes;
   cfg.stream = stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
@@ -287,7 +311,10 @@ cudaError_t launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorM
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  return cudaLaunchKernelEx(&cfg, mha::mha_fwd_kernel<D, CAUSAL, SPLIT, PAGED>, mq, mk, mv, prm);
+  using OArg = mha::OMapArg<mha::FwdCfg<D, SPLIT>::kOSets != 0>;
+  OArg oarg;
+  if constexpr (mha::FwdCfg<D, SPLIT>::kOSets != 0) oarg.map = mo;
+  return cudaLaunchKernelEx(&cfg, mha::mha_fwd_kernel<D, CAUSAL, SPLIT, PAGED, HMAJOR>, mq, mk, mv, oarg, prm);
 }
 
 }  // namespace
@@ -331,11 +358,19 @@ int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   const int rc = device_setup(&dev, &status);
   if (rc != MHA_OK) return rc;
 
-  CUtensorMap mq, mk, mv;
+  // at d = 128 O is written by TMA stores of 32-row boxes (one softmax
+  // warp's rows); at d = 64 the kernel stores O directly and gets the Q map
+  // in the O map's place, which it never uses
+  CUtensorMap mq, mk, mv, mo;
   if (!encode_map(&mq, q, static_cast<int>(BH), N, d, 128) ||
       !encode_map(&mk, k, static_cast<int>(BH), N, d, 128) ||
       !encode_map(&mv, v, static_cast<int>(BH), N, d, 128))
     return MHA_ERR_CUDA;
+  if (d == 128) {
+    if (!encode_map(&mo, o, static_cast<int>(BH), N, d, 32)) return MHA_ERR_CUDA;
+  } else {
+    mo = mq;
+  }
 
   mha::FwdParams prm = {};
   prm.o = static_cast<__nv_bfloat16*>(o);
@@ -350,11 +385,14 @@ int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t err;
   if (d == 64)
-    err = causal ? launch<64, true>(mq, mk, mv, prm, sms, st)
-                 : launch<64, false>(mq, mk, mv, prm, sms, st);
+    err = causal ? launch<64, true>(mq, mk, mv, mo, prm, sms, st)
+                 : launch<64, false>(mq, mk, mv, mo, prm, sms, st);
+  else if (use_head_major(static_cast<int>(BH), N, d, causal != 0, sms))
+    err = causal ? launch<128, true, false, false, true>(mq, mk, mv, mo, prm, sms, st)
+                 : launch<128, false, false, false, true>(mq, mk, mv, mo, prm, sms, st);
   else
-    err = causal ? launch<128, true>(mq, mk, mv, prm, sms, st)
-                 : launch<128, false>(mq, mk, mv, prm, sms, st);
+    err = causal ? launch<128, true>(mq, mk, mv, mo, prm, sms, st)
+                 : launch<128, false>(mq, mk, mv, mo, prm, sms, st);
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 

@@ -29,7 +29,8 @@
 //   warps 8-11  row per thread), softmax warpgroup for Q tile 1.  Each reads
 //               its S row from TMEM, masks, updates m and l, writes P (bf16)
 //               back over S, rescales O in TMEM when its max moved (the
-//               correction stage), and finally writes O / l and the LSE.
+//               correction stage), and finally writes O / l and the LSE
+//               (at d = 128 through a shared-memory chunk and TMA stores).
 //   warp 3      idle (keeps the softmax warpgroups aligned to TMEM lanes).
 // The two Q tiles ping-pong: while one softmax warpgroup works on its S, the
 // tensor core runs the other tile's GEMMs (the cooperative M-split of the
@@ -93,7 +94,7 @@ struct FwdParams {
   int* tile_counter;       // split mode: work tiles handed out so far past the grid (zero at launch)
 };
 
-template <int D>
+template <int D, bool SPLIT = false>
 struct FwdCfg {
   static_assert(D == 64 || D == 128, "head dimension");
   static constexpr int kBlockM = 128;  // query rows per softmax warpgroup
@@ -104,22 +105,32 @@ struct FwdCfg {
   static constexpr int kStages = (D == 128) ? 4 : 8;
   // Q buffer sets: with two, the next work tile's Q loads during this one
   static constexpr int kQSets = (D == 128) ? 1 : 2;
+  // square mode at d = 128: staging for the O epilogue, one 32-row chunk per
+  // TMEM lane quarter, written to HBM by TMA stores; the warps of the two
+  // stages on that lane quarter share it, in the order of their epilogues
+  // (there is no room for a chunk per warp).  At d = 64 the softmax warps
+  // store their rows directly, which measured faster there (2-4%) while the
+  // staged stores gained 1-2% at d = 128.
+  static constexpr int kOSets = (SPLIT || D == 64) ? 0 : 1;
+  static constexpr int kOChunkBytes = 32 * D * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQSets * 2 * kTileBytes;
-  static constexpr int kOffBar = kOffKV + kStages * kTileBytes;
+  static constexpr int kOffO = kOffKV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffO + kOSets * 4 * kOChunkBytes;
   // split mode: ring of work-tile ids from the K/V producer to the other
   // roles (Q producer, MMA issuer, the softmax warps that hold query rows)
   static constexpr int kTileRing = 8;
   // barriers: q_full[2] q_empty[2] kv_full[S] kv_empty[S] s_full[2] p_ready[2] o_full[2] drain
   // tail (paged mode: the copy of a V tile whose last rows get cleared)
-  // tile_full[R] tile_empty[R]
-  static constexpr int kNumBars = 4 + 2 * kStages + 2 + 2 + 2 + 1 + 1 + 2 * kTileRing;
+  // tile_full[R] tile_empty[R] o_free[4] (a shared O staging chunk is free)
+  static constexpr int kNumBars = 4 + 2 * kStages + 2 + 2 + 2 + 1 + 1 + 2 * kTileRing + 4;
   static constexpr int kOffTileIds = kOffBar + 8 * kNumBars;
   static constexpr int kOffTmemSlot = kOffTileIds + 4 * kTileRing;
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static_assert(kOffBar % 8 == 0 && kOffKV % 1024 == 0, "mbarrier / swizzle-atom alignment");
+  static_assert(kOffBar % 8 == 0 && kOffKV % 1024 == 0 && kOffO % 1024 == 0,
+                "mbarrier / swizzle-atom alignment");
   static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO0 = 256, kColO1 = 384;
@@ -127,6 +138,16 @@ struct FwdCfg {
   // by more than this many powers of two; P stays <= 2^8 meanwhile.
   static constexpr float kRescaleThreshold = 8.0f;
 };
+
+// The O tensor map: a kernel argument of the d = 128 square pass only (the
+// others store O with plain stores, and a larger argument block measured
+// slower on short launches).
+template <bool kHave>
+struct OMapArg {
+  CUtensorMap map;
+};
+template <>
+struct OMapArg<false> {};
 
 // Work tile u (0 <= u < BH * num_mblocks) is m-block r = u / BH of head
 // bh = u % BH, m-blocks heaviest first under the causal mask.  CTA c of G
@@ -156,12 +177,14 @@ __global__ void split_counter_reset_kernel(int* counter) {
 // d = 64 as 4-D [blocks][heads][page rows][d]; at d = 128 as 5-D
 // [blocks * heads][8-row group][d-half][row][64], which brings both
 // d-halves of a box's rows in one copy.
-template <int D, bool CAUSAL, bool SPLIT = false, bool PAGED = false>
-__global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
+template <int D, bool CAUSAL, bool SPLIT = false, bool PAGED = false, bool HMAJOR = false>
+__global__ void __launch_bounds__(FwdCfg<D, SPLIT>::kThreads, 1)
     mha_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<D>;
+                   const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ OMapArg<FwdCfg<D, SPLIT>::kOSets != 0> tmO, const FwdParams p) {
+  using C = FwdCfg<D, SPLIT>;
   static_assert(SPLIT || !PAGED, "the paged pass is a split pass");
+  static_assert(!(SPLIT && HMAJOR), "the head-major order is one of the square pass");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = ptx::smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -204,15 +227,38 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   };
   // square mode: the k-th tile of this CTA in the static order
   auto tile_at = [&](int k, Tile& t) -> bool {
-    const int u = fwd_tile_of_round(k, c, G);
-    if (u >= total) return false;
-    t.bh = u % p.BH;
     t.nk = N;
     t.split = 0;
     t.kv_begin = 0;
-    const int r = u / p.BH;
-    const int mblk = CAUSAL ? (p.num_mblocks - 1 - r) : r;
-    t.m0 = mblk * 256;
+    if constexpr (HMAJOR) {
+      // Head-major order: CTA c takes items c, c + G, c + 2G, ...; the items
+      // of one head are adjacent, so the grid works on a few heads' K/V at a
+      // time and they stay in L2.  Under the causal mask item i of a head is
+      // the pair of m-blocks M-1-i (first) and i, whose K/V tile counts add
+      // up to the same M + 1 for every pair, so the rounds stay balanced; the
+      // middle m-block of an odd M has no partner, and its second tile is
+      // empty (placed past the end).
+      const int per_head = CAUSAL ? (p.num_mblocks + 1) >> 1 : p.num_mblocks;
+      const int w = c + (CAUSAL ? (k >> 1) : k) * G;
+      if (w >= p.BH * per_head) return false;
+      t.bh = w / per_head;
+      const int i = w - t.bh * per_head;
+      int mblk = i;
+      bool empty = false;
+      if constexpr (CAUSAL) {
+        const int hi = p.num_mblocks - 1 - i;
+        mblk = (k & 1) ? i : hi;
+        empty = (k & 1) && hi == i;
+      }
+      t.m0 = empty ? N : mblk * 256;
+    } else {
+      const int u = fwd_tile_of_round(k, c, G);
+      if (u >= total) return false;
+      t.bh = u % p.BH;
+      const int r = u / p.BH;
+      const int mblk = CAUSAL ? (p.num_mblocks - 1 - r) : r;
+      t.m0 = mblk * 256;
+    }
     t.n0 = tiles_for(t.m0);
     t.n1 = tiles_for(t.m0 + C::kBlockM);
     t.nkv = max(t.n0, t.n1);  // both stages read the same K/V tiles
@@ -237,6 +283,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
   const uint32_t tail_bar = bar(11 + 2 * C::kStages);
   auto tile_full = [&](int i) { return bar(12 + 2 * C::kStages + i); };
   auto tile_empty = [&](int i) { return bar(12 + 2 * C::kStages + C::kTileRing + i); };
+  auto o_free = [&](int i) { return bar(12 + 2 * C::kStages + 2 * C::kTileRing + i); };
   int* tile_ids = reinterpret_cast<int*>(smem + C::kOffTileIds);
   // Q tile of set b, stage s
   auto q_index = [](int b, int s) { return SPLIT ? b : 2 * b + s; };
@@ -304,6 +351,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       ptx::mbar_init(tile_full(i), 1);
       ptx::mbar_init(tile_empty(i), 2 + 2 * p_arrivals);  // one arrive per consumer warp
     }
+    for (int i = 0; i < 4; ++i) ptx::mbar_init(o_free(i), 1);
     *abort_flag = 0;
     ptx::fence_barrier_init();
   }
@@ -311,6 +359,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     ptx::prefetch_tensormap(&tmQ);
     ptx::prefetch_tensormap(&tmK);
     ptx::prefetch_tensormap(&tmV);
+    if constexpr (C::kOSets > 0) ptx::prefetch_tensormap(&tmO.map);
   }
   if (warp == 1) {
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
@@ -696,6 +745,7 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
     bool ok = true;
     int sf = 0;  // s_full completions consumed
     int of = 0;  // o_full completions consumed
+    int ouse = 0;  // square mode: epilogues on this warp's staging chunk so far
     Tile tl;
     // split mode: the Nq <= 32 query rows lie in the first warp of each
     // stage; the other softmax warps have no work and go straight to the
@@ -706,6 +756,13 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
       const int m0 = tl.m0;
       const int n = s ? tl.n1 : tl.n0;
       const int q_idx = SPLIT ? row : m0 + s * C::kBlockM + row;
+      // square mode: this work tile's use of the staging chunk (d = 128:
+      // the chunk is shared, stage 0's epilogue of a work tile comes first)
+      int my_use = 0;
+      if constexpr (C::kOSets > 0) {
+        my_use = ouse + ((s == 1 && tl.n0 > 0) ? 1 : 0);
+        ouse += (tl.n0 > 0 ? 1 : 0) + (tl.n1 > 0 ? 1 : 0);
+      }
       float m_run = -INFINITY;  // running max of scale*log2(e)*s, possibly stale
       float l_run = 0.f;   // row sum of exp2 terms (fp32), for the LSE
       float lr_run = 0.f;  // the same over the bf16-rounded terms, for O
@@ -766,6 +823,8 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
             sum2[i & 1] = __fadd2_rn(sum2[i & 1], make_float2(p0, p1));
             // normalising O by the sum of the bf16 values the tensor core
             // multiplies into V keeps O an exact convex combination of V rows
+            // (a row that one key dominates reproduces that key's V row even
+            // when the running max is stale and that key's P is rounded)
             sumr[(2 * i) & 3] = ptx::add_bf16_lo(pk[i], sumr[(2 * i) & 3]);
             sumr[(2 * i + 1) & 3] = ptx::add_bf16_hi(pk[i], sumr[(2 * i + 1) & 3]);
           }
@@ -843,27 +902,72 @@ __global__ void __launch_bounds__(FwdCfg<D>::kThreads, 1)
         ptx::tc_fence_before();
         continue;
       }
-      const bool valid = q_idx < N;
-      __nv_bfloat16* orow = p.o + (static_cast<size_t>(tl.bh) * N + (valid ? q_idx : 0)) * D;
+      if constexpr (C::kOSets > 0) {
+        // square mode: O / l in bf16 into this warp's staging chunk, laid out
+        // as the O tensor map's 128-byte swizzle expects (16-byte piece c of
+        // row r at position c ^ (r mod 8) of the row), then one TMA store per
+        // d-half of the warp's 32 rows; rows past N are not written
+        const uint32_t chunk = sbase + C::kOffO + wq * C::kOChunkBytes;
+        // the other stage's warp on this lane quarter is done with the chunk
+        if (my_use > 0 && !wait_warp(o_free(wq), (my_use - 1) & 1, ctl, kSiteSoftmaxO)) {
+          ok = false;
+          break;
+        }
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t ov[32];
-        ptx::tmem_ld_x32(t_o + cc * 32, ov);
-        uint32_t pk[16];
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          ptx::tmem_ld_x32(t_o + cc * 32, ov);
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
-                                   __uint_as_float(ov[2 * i + 1]) * inv_l);
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+          for (int i = 0; i < 16; ++i)
+            pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                     __uint_as_float(ov[2 * i + 1]) * inv_l);
 #pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4)
-            dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          for (int v4 = 0; v4 < 4; ++v4) {
+            const int piece = cc * 4 + v4;  // 16-byte piece (8 columns) of the row
+            const uint32_t addr = chunk + (piece >> 3) * 4096 + lane * 128 + (((piece & 7) ^ (lane & 7)) << 4);
+            ptx::st_shared_v4(addr, pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
+        }
+        ptx::fence_proxy_async_smem();  // the chunk is read by the async proxy
+        __syncwarp();
+        const int row0 = m0 + s * C::kBlockM + wq * 32;  // this warp's first row
+        if (lane == 0) {
+          if (row0 < N) {
+#pragma unroll
+            for (int h = 0; h < C::kHalves; ++h) ptx::tma_store_3d(&tmO.map, chunk + h * 4096, h * 64, row0, tl.bh);
+            ptx::bulk_commit_group();
+          }
+          ptx::bulk_wait_read_all();
+          ptx::mbar_arrive(o_free(wq));
+        }
+        __syncwarp();
+      } else {
+        const bool valid = q_idx < N;
+        __nv_bfloat16* orow = p.o + (static_cast<size_t>(tl.bh) * N + (valid ? q_idx : 0)) * D;
+#pragma unroll
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          ptx::tmem_ld_x32(t_o + cc * 32, ov);
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = ptx::pack_bf16x2(__uint_as_float(ov[2 * i]) * inv_l,
+                                     __uint_as_float(ov[2 * i + 1]) * inv_l);
+          if (valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int v4 = 0; v4 < 4; ++v4)
+              dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+          }
         }
       }
-      if (valid) p.lse[static_cast<size_t>(tl.bh) * N + q_idx] = lse_row;
+      if (q_idx < N) p.lse[static_cast<size_t>(tl.bh) * N + q_idx] = lse_row;
       ptx::tc_fence_before();
     }
+    // the O stores complete before the CTA (and its shared memory) goes away
+    if (C::kOSets > 0 && lane == 0) ptx::bulk_wait_all();
+    __syncwarp();
   }
 
   ptx::tc_fence_before();

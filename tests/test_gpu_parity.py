@@ -109,3 +109,44 @@ def test_sharp_softmax_rescaling(d):
         o, lse = run_gpu(q, k, v, causal)
         o_ref, lse_ref = oracle.attention_fwd(q, k, v, scale_for(d), causal)
         assert_close(o, lse, o_ref, lse_ref, f"sharp d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("shape", [(1, 32, 16603, True), (2, 32, 4000, False)],
+                         ids=["causal-odd-mblocks", "noncausal-ragged"])
+def test_head_major_order(shape):
+    """Shapes whose K/V exceed L2 at d = 128 run the head-major tile order
+    (causal: pairs of m-blocks M-1-i and i per CTA).  N = 16603 gives an odd
+    m-block count (65: the middle m-block's partner is an empty tile) and a
+    ragged last tile; N = 4000 is the non-causal form with a ragged tail.
+    Sampled rows of several heads against the oracle, including the middle
+    m-block and the last rows, plus finiteness and the convex-hull bound on
+    every output."""
+    import torch
+    B, H, N, causal = shape
+    d = 128
+    q, k, v = synth.qkv(31 + N, B, H, N, d)
+    o, lse = run_gpu(q, k, v, causal)
+    rng = np.random.default_rng(N)
+    mid = (((N + 255) // 256) // 2) * 256
+    fixed = [0, 1, 255, 256, mid - 1, mid, mid + 127, mid + 128, mid + 255, N - 129, N - 128, N - 2, N - 1]
+    heads = np.unique(np.concatenate([[0, B * H - 1], rng.integers(0, B * H, 3)]))
+    o_all, l_all, o_ref_all, l_ref_all = [], [], [], []
+    for bh in heads:
+        rows = np.unique(np.clip(np.array(fixed + rng.integers(0, N, 24).tolist()), 0, N - 1))
+        o_ref, lse_ref = oracle.attention_rows(q, k, v, scale_for(d), causal, int(bh), rows)
+        o_all.append(o.reshape(B * H, N, d)[bh][rows])
+        l_all.append(lse.reshape(B * H, N)[bh][rows])
+        o_ref_all.append(o_ref)
+        l_ref_all.append(lse_ref)
+    assert_close(np.concatenate(o_all), np.concatenate(l_all), np.concatenate(o_ref_all),
+                 np.concatenate(l_ref_all), f"head-major {shape}")
+    vt = torch.from_numpy(synth.bf16_bits_to_f32(v)).cuda().reshape(B * H, N, d)
+    ot = torch.from_numpy(o).cuda().reshape(B * H, N, d).float()
+    if causal:
+        hi, lo = torch.cummax(vt, dim=1).values, torch.cummin(vt, dim=1).values
+    else:
+        hi = vt.amax(dim=1, keepdim=True).expand_as(vt)
+        lo = vt.amin(dim=1, keepdim=True).expand_as(vt)
+    slack = 1e-2 + 1e-2 * vt.abs().amax()
+    assert bool(((ot <= hi + slack) & (ot >= lo - slack)).all())
+    assert np.isfinite(lse).all()

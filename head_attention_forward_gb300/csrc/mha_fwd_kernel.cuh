@@ -102,7 +102,13 @@ struct FwdCfg {
   static constexpr int kHalves = D / 64;  // 128-byte swizzle atoms across d
   static constexpr int kHalfBytes = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int kTileBytes = kHalves * kHalfBytes;
-  static constexpr int kStages = (D == 128) ? 4 : 8;
+  // square mode at d = 64: the tensor core also sums each row's bf16 P: the
+  // V operand of P V gets a 65th column of ones, read from a constant tile
+  // after the ring (its descriptor's N-atom stride points there), and O(s)
+  // holds that sum in column 64
+  static constexpr bool kSumCol = !SPLIT && D == 64;
+  static constexpr int kONcols = kSumCol ? 80 : D;  // P V's N (a multiple of 16)
+  static constexpr int kStages = (D == 128) ? 4 : (kSumCol ? 7 : 8);
   // Q buffer sets: with two, the next work tile's Q loads during this one
   static constexpr int kQSets = (D == 128) ? 1 : 2;
   // square mode at d = 128: staging for the O epilogue, one 32-row chunk per
@@ -116,7 +122,9 @@ struct FwdCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQSets * 2 * kTileBytes;
   static constexpr int kOffO = kOffKV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffO + kOSets * 4 * kOChunkBytes;
+  // the ones tile: 128 keys x one 128-byte swizzle row, 8-key groups 1 KiB apart
+  static constexpr int kOffOnes = kOffO + kOSets * 4 * kOChunkBytes;
+  static constexpr int kOffBar = kOffOnes + (kSumCol ? 16 * 1024 : 0);
   // split mode: ring of work-tile ids from the K/V producer to the other
   // roles (Q producer, MMA issuer, the softmax warps that hold query rows)
   static constexpr int kTileRing = 8;
@@ -129,7 +137,7 @@ struct FwdCfg {
   static constexpr int kOffAbort = kOffTmemSlot + 4;
   static constexpr int kSmemBytes = kOffAbort + 4 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
-  static_assert(kOffBar % 8 == 0 && kOffKV % 1024 == 0 && kOffO % 1024 == 0,
+  static_assert(kOffBar % 8 == 0 && kOffKV % 1024 == 0 && kOffO % 1024 == 0 && kOffOnes % 1024 == 0,
                 "mbarrier / swizzle-atom alignment");
   static constexpr int kThreads = 384;
   static constexpr uint32_t kTmemCols = 512;
@@ -365,6 +373,18 @@ __global__ void __launch_bounds__(FwdCfg<D, SPLIT>::kThreads, 1)
     ptx::tmem_alloc(ptx::smem_u32(tmem_slot), C::kTmemCols);
     ptx::tmem_relinquish();
   }
+  if constexpr (C::kSumCol) {
+    // the ones tile in the V tiles' layout (MN-major, 128-byte swizzle): key
+    // k's row holds bf16 1.0 at N-position 0 of the atom, i.e. in 16-byte
+    // piece 0 ^ (k mod 8), and zeros elsewhere; thread k < 128 writes row k
+    if (threadIdx.x < 128) {
+      const int k = threadIdx.x;
+      uint4* row = reinterpret_cast<uint4*>(smem + C::kOffOnes + (k >> 3) * 1024 + (k & 7) * 128);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) row[c] = make_uint4(c == (k & 7) ? 0x3F80u : 0u, 0u, 0u, 0u);
+      ptx::fence_proxy_async_smem();  // read by the tensor core
+    }
+  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
@@ -582,7 +602,7 @@ __global__ void __launch_bounds__(FwdCfg<D, SPLIT>::kThreads, 1)
     // ---------------------------------------------------------- MMA issuer
     {
       constexpr uint32_t kIdescS = ptx::idesc_bf16_f32(128, C::kBlockN, 0, 0);
-      constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(128, D, 0, 1);
+      constexpr uint32_t kIdescO = ptx::idesc_bf16_f32(128, C::kONcols, 0, 1);
       const uint32_t tS0 = tmem + C::kColS0, tS1 = tmem + C::kColS1;
       const uint32_t tO0 = tmem + C::kColO0, tO1 = tmem + C::kColO1;
       // Descriptors are built once; moving to another slot or k-step only
@@ -598,9 +618,18 @@ __global__ void __launch_bounds__(FwdCfg<D, SPLIT>::kThreads, 1)
       const uint64_t dK0 = ptx::desc_sw128(sKV(0), 16, kKVGroupBytes);
       // V tiles: MN-major (d contiguous), d-halves kKVHalfBytes apart (LBO),
       // 8-key groups kKVGroupBytes apart (SBO).
-      const uint64_t dV0 = ptx::desc_sw128(sKV(0), kKVHalfBytes, kKVGroupBytes);
+      // With the sum column, N-atom 1 of every slot's V is the ones tile: the
+      // stride field holds (ones - slot) >> 4, so moving to slot i adds
+      // i * tile >> 4 to the start field and takes it off the stride field
+      // (which stays positive: the ones tile lies past the ring).
+      const uint64_t dV0 =
+          ptx::desc_sw128(sKV(0), C::kSumCol ? sbase + C::kOffOnes - sKV(0) : kKVHalfBytes, kKVGroupBytes);
       auto slot_off = [](int slot) -> uint64_t {
         return static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
+      };
+      auto v_off = [](int slot) -> uint64_t {
+        const uint64_t a = static_cast<uint64_t>((slot * C::kTileBytes) >> 4);
+        return C::kSumCol ? a - (a << 16) : a;
       };
       // S(s) = Q_s K^T over K = d in steps of 16
       auto issue_s = [&](int qb, int s, int kslot) {
@@ -622,7 +651,7 @@ __global__ void __launch_bounds__(FwdCfg<D, SPLIT>::kThreads, 1)
       // O(so) += P V over 128 keys in steps of 16; P read from TMEM, from
       // the S columns of stage sp
       auto issue_pv_from = [&](int sp, int so, int vslot, bool first) {
-        const uint64_t dv = dV0 + slot_off(vslot);
+        const uint64_t dv = dV0 + v_off(vslot);
         const uint32_t ts = sp ? tS1 : tS0;
         const uint32_t to = so ? tO1 : tO0;
         if (ptx::elect_one()) {
@@ -825,8 +854,10 @@ __global__ void __launch_bounds__(FwdCfg<D, SPLIT>::kThreads, 1)
             // multiplies into V keeps O an exact convex combination of V rows
             // (a row that one key dominates reproduces that key's V row even
             // when the running max is stale and that key's P is rounded)
-            sumr[(2 * i) & 3] = ptx::add_bf16_lo(pk[i], sumr[(2 * i) & 3]);
-            sumr[(2 * i + 1) & 3] = ptx::add_bf16_hi(pk[i], sumr[(2 * i + 1) & 3]);
+            if constexpr (!C::kSumCol) {
+              sumr[(2 * i) & 3] = ptx::add_bf16_lo(pk[i], sumr[(2 * i) & 3]);
+              sumr[(2 * i + 1) & 3] = ptx::add_bf16_hi(pk[i], sumr[(2 * i + 1) & 3]);
+            }
           }
           ptx::tmem_st_x16(t_s + c4 * 16, pk);
         }
@@ -842,6 +873,8 @@ __global__ void __launch_bounds__(FwdCfg<D, SPLIT>::kThreads, 1)
             for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
             ptx::tmem_st_x32(t_o + cc * 32, ov);
           }
+          if constexpr (C::kSumCol)
+            ptx::tmem_st_x1(t_o + D, __float_as_uint(__uint_as_float(ptx::tmem_ld_x1(t_o + D)) * alpha));
         }
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -874,6 +907,7 @@ __global__ void __launch_bounds__(FwdCfg<D, SPLIT>::kThreads, 1)
       // epilogue: O = O_acc / l in bf16, LSE = (m + log2 l) * ln 2.  The next
       // work tile's first P V overwrites O(s) only after this warp's next
       // p_ready arrival, which follows these reads.
+      if constexpr (C::kSumCol) lr_run = __uint_as_float(ptx::tmem_ld_x1(t_o + D));  // the tensor core's sum
       const float inv_l = lr_run > 0.f ? 1.f / lr_run : 0.f;
       const float m_fin = (m_run == -INFINITY) ? 0.f : m_run;
       const float lse_row = l_run > 0.f ? (m_fin + log2f(l_run)) * 0.69314718055994530942f : -INFINITY;

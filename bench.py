@@ -60,6 +60,20 @@ def counted_flops(c) -> float:
     return f / 2 if c["causal"] else f
 
 
+def fwd_kernel_name(B, H, N, d, causal, sms) -> str:
+    """The forward instantiation mha_fwd launches for a shape: the
+    library's tile-order rule restated (the head-major order at d = 128 once
+    all heads' K/V exceed 96 MiB and its rounds of equal work items fill at
+    least 95% of the grid's slots), for labelling the measurements."""
+    BH = B * H
+    mblocks = (N + 255) // 256
+    items = BH * ((mblocks + 1) // 2 if causal else mblocks)
+    grid = min(items, sms)
+    rounds = -(-items // grid)
+    hmajor = d == 128 and 2 * BH * N * d * 2 > 96 * 2**20 and items >= 0.95 * rounds * grid
+    return f"mha_fwd_kernel<{d},{'true' if causal else 'false'}{',head-major' if hmajor else ''}>"
+
+
 def workload_name(name, c) -> str:
     return (f"{name}: B={c['B']},H={c['H']},N={c['N']},d={c['d']},"
             f"{'causal' if c['causal'] else 'non-causal'}")
@@ -94,10 +108,11 @@ def pick_peak(region_s: float):
     return sustained, f"{src} bf16_tflops_sustained (timed region {region_s:.3f} s >= {BURST_REGION_S:.0f} s)"
 
 
-# Source files each kernel is compiled from; a recorded ncu traffic figure is
-# valid only while these are unchanged.
+# Source files each kernel is compiled from (and the host file that picks
+# its launch shape and tile order); a recorded ncu traffic figure is valid
+# only while these are unchanged.
 KERNEL_SOURCES = {
-    "mha_fwd_kernel": ("mha_fwd_kernel.cuh", "sm103_ptx.cuh", "mha_wait.cuh"),
+    "mha_fwd_kernel": ("mha_fwd_kernel.cuh", "sm103_ptx.cuh", "mha_wait.cuh", "mha_fwd.cu"),
 }
 
 
@@ -533,6 +548,73 @@ def run_paged(args, name):
     }), flush=True)
     return 0
 
+def run_page_sweep(args):
+    """The paged-KV path against page size: one query per sequence, 32
+    sequences of 8192 keys each, 32 heads, d = 128 (a 1.07 GB cache), with the
+    pages in sequence order (identity table) and shuffled over the cache.
+    Prints one JSON line: per page size and table, the call time and the
+    achieved fraction of the measured HBM copy rate."""
+    import torch
+
+    import head_attention_forward_gb300 as mha
+    torch.cuda.set_device(0)
+    mha.build()
+    mha.lib()
+    B, H, Nq, d, keys = 32, 32, 1, 128, 8192
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    stream = torch.cuda.current_stream()
+    sptr = int(stream.cuda_stream)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(12)
+    q = torch.randn((B, H, Nq, d), generator=gen, device="cuda").to(torch.bfloat16)
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, Nq), dtype=torch.float32, device="cuda")
+    seq = torch.full((B,), keys, dtype=torch.int32, device="cuda")
+    peak, src = hbm_peak_gbs()
+    rows = []
+    for page in (16, 32, 64, 128, 256):
+        pages = keys // page
+        num_blocks = B * pages
+        kc = torch.randn((num_blocks, H, page, d), generator=gen, device="cuda").to(torch.bfloat16)
+        vc = torch.randn((num_blocks, H, page, d), generator=gen, device="cuda").to(torch.bfloat16)
+        ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, keys, d, 0)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        for order in ("identity", "shuffled"):
+            ids = torch.arange(num_blocks, dtype=torch.int32, device="cuda")
+            if order == "shuffled":
+                ids = ids[torch.randperm(num_blocks, generator=gen, device="cuda")]
+            table = ids.reshape(B, pages).contiguous()
+
+            def step():
+                mha.mha_fwd_paged(q, kc, vc, table, seq, o, lse, B, H, Nq, d, page, num_blocks, pages,
+                                  scale, False, 0, ws, ws_bytes, sptr)
+
+            for _ in range(max(args.warmup, 3)):
+                step()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with NvmlSampler(0) as nv:
+                nv.mark()
+                e0.record(stream)
+                for _ in range(args.steps):
+                    step()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                nv.mark()
+            rc, word = mha.mha_device_status(sptr)
+            if rc != mha.MHA_OK:
+                raise RuntimeError(f"page {page}: device status {rc} ({word:#x})")
+            ms = e0.elapsed_time(e1) / args.steps
+            algo = 2 * 2 * B * H * keys * d + 2 * (q.numel() + o.numel()) + 4 * lse.numel() + 4 * table.numel() + 4 * B
+            gbs = algo / (ms / 1e3) / 1e9
+            rows.append({"page": page, "table": order, "ms": ms, "gbs": gbs, "frac": gbs / peak,
+                         "clocks": nv.summary()})
+        del kc, vc, ws
+    print(json.dumps({"mode": "page_sweep", "workload": f"B={B},H={H},Nq={Nq},d={d},{keys} keys per sequence",
+                      "steps": args.steps, "peak_gbs": peak, "peak_source": src, "rows": rows}), flush=True)
+    return 0
+
+
 _INPUT_CACHE = {}
 
 
@@ -620,7 +702,7 @@ def time_forward_config(mha, name, dev, stream, min_steps: int, min_region_s: fl
             "peak": peak, "peak_source": peak_src, "pct_of_burst_peak": 100.0 * tf / peak_burst,
             "ms_per_launch": ms, "median_launch_ms": statistics.median(per), "steps": steps,
             "timing": timing, "clocks": clocks,
-            "kernel": f"mha_fwd_kernel<{d},{'true' if causal else 'false'}>"}
+            "kernel": fwd_kernel_name(B, H, N, d, causal, torch.cuda.get_device_properties(dev).multi_processor_count)}
 
 
 BWD_METRIC = ("attention bwd TFLOP/s (counted 10*B*H*N^2*d, halved when causal) and % of GB300 "
@@ -718,7 +800,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--backward", action="store_true",
                     help="time mha_bwd on the chosen forward workload instead of mha_fwd")
+    ap.add_argument("--page-sweep", action="store_true",
+                    help="time the paged-KV path at page sizes 16..256, pages in order and shuffled")
     args = ap.parse_args()
+    if args.page_sweep:
+        return run_page_sweep(args)
     name = args.config
     if args.backward:
         if name not in synth.CONFIGS:
@@ -929,7 +1015,8 @@ def main():
                          "peak_sustained": peak_sustained, "frac_sustained": achieved / peak_sustained,
                          "traffic": recorded_traffic(name),
                          "algorithmic_flops_per_launch": flops,
-                         "kernel": f"mha_fwd_kernel<{d},{'true' if causal else 'false'}>"},
+                         "kernel": fwd_kernel_name(B, H, N, d, causal,
+                                                   torch.cuda.get_device_properties(dev).multi_processor_count)},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                     "pipelined": "two device buffer sets; step k+1's upload and step k-1's "

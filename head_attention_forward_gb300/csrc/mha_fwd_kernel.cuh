@@ -108,7 +108,7 @@ struct FwdCfg {
   // holds that sum in column 64
   static constexpr bool kSumCol = !SPLIT && D == 64;
   static constexpr int kONcols = kSumCol ? 80 : D;  // P V's N (a multiple of 16)
-  static constexpr int kStages = (D == 128) ? 4 : (kSumCol ? 7 : 8);
+  static constexpr int kStages = (D == 128) ? 4 : 8;
   // Q buffer sets: with two, the next work tile's Q loads during this one
   static constexpr int kQSets = (D == 128) ? 1 : 2;
   // square mode at d = 128: staging for the O epilogue, one 32-row chunk per

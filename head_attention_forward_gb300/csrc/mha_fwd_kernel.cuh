@@ -13,6 +13,8 @@
 // head), split into two 128-row Q tiles.  The kernel is persistent: one CTA
 // per SM walks its share of the work tiles, so TMEM, barriers and the K/V
 // ring are set up once and the next tile's loads overlap this one's tail.
+// The work tiles come in snake rounds over heads, or (HMAJOR, d = 128 with
+// K/V beyond L2) head-major, causal m-blocks paired for equal cost.
 //   warp 0      TMA producer for K_j / V_j of every work tile in turn, into
 //               a ring of shared-memory stages guarded by full/empty
 //               mbarriers (the producer/consumer tokens of the Triton
@@ -36,8 +38,10 @@
 // tensor core runs the other tile's GEMMs (the cooperative M-split of the
 // warp-specialisation notes, one consumer group per half of the rows).
 //
-// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [384,384+D).
-// P_j(s) (128 keys as 64 packed bf16x2 columns) overwrites S(s) cols [0,64).
+// TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+W), O1 [384,384+W),
+// W = D, or 80 in the square pass at d = 64 (column 64 then holds the row
+// sum of P, formed by the tensor core).  P_j(s) (128 keys as 64 packed
+// bf16x2 columns) overwrites S(s) cols [0,64).
 // The tensor pipe executes one thread's MMAs in issue order, so issuing
 // S_{j+1}(s) after PV_j(s) cannot clobber P_j(s) before it is read.
 //

@@ -548,6 +548,85 @@ def run_paged(args, name):
     }), flush=True)
     return 0
 
+def time_decode_block(mha, dev, stream, steps: int):
+    """The split-KV and paged decode workloads for the default bench line,
+    each timed over `steps` back-to-back calls (counter reset, partial pass,
+    merge) after 3 warm-ups, against the measured HBM copy rate.  Their
+    shapes, masks and (paged) block tables and lengths are the parity
+    workloads'; the K/V values are seeded torch normals drawn on the device,
+    which times the same work without generating gigabytes on the host."""
+    import torch
+    peak, src = hbm_peak_gbs()
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(21)
+    sptr = int(stream.cuda_stream)
+
+    def randn(shape):
+        return torch.randn(shape, generator=gen, device=dev).to(torch.bfloat16)
+
+    def timed(step):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with NvmlSampler(dev.index) as nv:
+            nv.mark()
+            e0.record(stream)
+            for _ in range(steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            nv.mark()
+        rc, word = mha.mha_device_status(sptr)
+        if rc != mha.MHA_OK:
+            raise RuntimeError(f"device status {rc} ({word:#x})")
+        return e0.elapsed_time(e1) / steps, nv.summary()
+
+    out = {}
+    for name, c in synth.DECODE_CONFIGS.items():
+        B, H, Nq, Nk, d, causal = c["B"], c["H"], c["Nq"], c["Nk"], c["d"], c["causal"]
+        q, k, v = randn((B, H, Nq, d)), randn((B, H, Nk, d)), randn((B, H, Nk, d))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+        ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, Nk, d, 0)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        scale = float(np.float32(1.0 / math.sqrt(d)))
+        ms, clocks = timed(lambda: mha.mha_fwd_kv(q, k, v, o, lse, B, H, Nq, Nk, d, scale, causal, 0,
+                                                 ws, ws_bytes, sptr))
+        algo = 2 * (q.numel() + k.numel() + v.numel() + o.numel()) + 4 * lse.numel()
+        gbs = algo / (ms / 1e3) / 1e9
+        out[name] = {"workload": f"B={B},H={H},Nq={Nq},Nk={Nk},d={d},{'causal' if causal else 'non-causal'} "
+                                 "(split-KV path)",
+                     "ms_per_call": ms, "gbs": gbs, "frac": gbs / peak, "peak_gbs": peak, "peak_source": src,
+                     "algorithmic_bytes": algo, "steps": steps, "clocks": clocks,
+                     "kernel": f"mha_fwd_kernel<{d},{int(bool(causal))},split> + splitkv_merge_kernel<{d}>"}
+        del q, k, v, o, lse, ws
+    for name, c in synth.PAGED_CONFIGS.items():
+        B, H, Nq, d, page, causal = c["B"], c["H"], c["Nq"], c["d"], c["page"], c["causal"]
+        seq, table, num_blocks = synth.paged_layout(name)
+        max_blocks = table.shape[1]
+        q = randn((B, H, Nq, d))
+        kc, vc = randn((num_blocks, H, page, d)), randn((num_blocks, H, page, d))
+        td, sd = torch.from_numpy(table).to(dev), torch.from_numpy(seq).to(dev)
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Nq), dtype=torch.float32, device=dev)
+        ws_bytes = mha.mha_fwd_kv_workspace_size(B, H, Nq, max_blocks * page, d, 0)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        scale = float(np.float32(1.0 / math.sqrt(d)))
+        ms, clocks = timed(lambda: mha.mha_fwd_paged(q, kc, vc, td, sd, o, lse, B, H, Nq, d, page, num_blocks,
+                                                    max_blocks, scale, causal, 0, ws, ws_bytes, sptr))
+        keys = int(seq.astype(np.int64).sum())
+        algo = 2 * 2 * keys * H * d + 2 * (q.numel() + o.numel()) + 4 * lse.numel() + table.nbytes + seq.nbytes
+        gbs = algo / (ms / 1e3) / 1e9
+        out[name] = {"workload": f"B={B},H={H},Nq={Nq},d={d},page={page},seq {int(seq.min())}..{int(seq.max())} "
+                                 "(paged-KV path)",
+                     "ms_per_call": ms, "gbs": gbs, "frac": gbs / peak, "peak_gbs": peak, "peak_source": src,
+                     "algorithmic_bytes": algo, "steps": steps, "clocks": clocks,
+                     "kernel": f"mha_fwd_kernel<{d},{int(bool(causal))},split,paged> + splitkv_merge_kernel<{d}>"}
+        del q, kc, vc, td, sd, o, lse, ws
+    return out
+
+
 def run_page_sweep(args):
     """The paged-KV path against page size: one query per sequence, 32
     sequences of 8192 keys each, 32 heads, d = 128 (a 1.07 GB cache), with the
@@ -796,7 +875,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
-                    help="time only the chosen workload (no per_config block)")
+                    help="time only the chosen workload (no per_config or per_decode block)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--backward", action="store_true",
                     help="time mha_bwd on the chosen forward workload instead of mha_fwd")
@@ -914,11 +993,13 @@ def main():
         clocks["cycles_per_launch"] = mean_launch_ms * 1e-3 * clocks["sm_mhz"] * 1e6
 
     per_config = None
+    per_decode = None
     if world == 1 and not args.no_per_config:
         per_config = {}
         for other in synth.CONFIGS:
             if other != name:
                 per_config[other] = time_forward_config(mha, other, dev, stream, args.steps)
+        per_decode = time_decode_block(mha, dev, stream, 50)
 
     # End to end through the public C ABI: every step copies its Q, K, V from
     # pinned host memory to the device, runs mha_fwd, and copies O and LSE
@@ -1028,6 +1109,8 @@ def main():
         }
         if per_config is not None:
             line["per_config"] = per_config
+        if per_decode is not None:
+            line["per_decode"] = per_decode
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

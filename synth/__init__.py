@@ -201,11 +201,12 @@ PAGED_CONFIGS = {
 }
 
 
-def paged_inputs(name: str):
-    """q [B,H,Nq,d], k/v caches [num_blocks,H,page,d] (bf16 bits), block table
-    [B, max_blocks] int32 (pages shuffled over the cache) and seq_lens [B]."""
+def paged_layout(name: str):
+    """The paged workload's sequence lengths [B] (int32), block table
+    [B, max_blocks] (int32, pages shuffled over the cache, unused entries
+    -1) and cache size in blocks, without the cache itself."""
     c = PAGED_CONFIGS[name]
-    B, H, Nq, d, page = c["B"], c["H"], c["Nq"], c["d"], c["page"]
+    B, page = c["B"], c["page"]
     w = words(c["seed"], 3, 0, B)  # stream 3: sequence lengths and page placement
     span = c["hi"] - c["lo"] + 1
     seq = (c["lo"] + (w % np.uint64(span)).astype(np.int64)).astype(np.int32)
@@ -218,6 +219,15 @@ def paged_inputs(name: str):
     for b in range(B):
         table[b, :pages[b]] = order[pos:pos + pages[b]]
         pos += int(pages[b])
+    return seq, table, num_blocks
+
+
+def paged_inputs(name: str):
+    """q [B,H,Nq,d], k/v caches [num_blocks,H,page,d] (bf16 bits), block table
+    [B, max_blocks] int32 (pages shuffled over the cache) and seq_lens [B]."""
+    c = PAGED_CONFIGS[name]
+    B, H, Nq, d, page = c["B"], c["H"], c["Nq"], c["d"], c["page"]
+    seq, table, num_blocks = paged_layout(name)
     gen = normal_bf16_c
     q = gen(c["seed"], STREAM_Q, B * H * Nq * d).reshape(B, H, Nq, d)
     kc = gen(c["seed"], STREAM_K, num_blocks * H * page * d).reshape(num_blocks, H, page, d)

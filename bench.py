@@ -61,16 +61,11 @@ def counted_flops(c) -> float:
 
 
 def fwd_kernel_name(B, H, N, d, causal, sms) -> str:
-    """The forward instantiation mha_fwd launches for a shape: the
-    library's tile-order rule restated (the head-major order at d = 128 once
-    all heads' K/V exceed 96 MiB and its rounds of equal work items fill at
-    least 95% of the grid's slots), for labelling the measurements."""
-    BH = B * H
-    mblocks = (N + 255) // 256
-    items = BH * ((mblocks + 1) // 2 if causal else mblocks)
-    grid = min(items, sms)
-    rounds = -(-items // grid)
-    hmajor = d == 128 and 2 * BH * N * d * 2 > 96 * 2**20 and items >= 0.95 * rounds * grid
+    """The forward instantiation mha_fwd launches for a shape on a device
+    with `sms` multiprocessors, as the library reports its tile order, for
+    labelling the measurements."""
+    import head_attention_forward_gb300 as mha
+    hmajor = mha.mha_fwd_tile_order(B, H, N, d, causal, sms) == 1
     return f"mha_fwd_kernel<{d},{'true' if causal else 'false'}{',head-major' if hmajor else ''}>"
 
 

@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.mha_bwd.restype = i
         L.mha_bwd_workspace_size.argtypes = [i, i, i, i]
         L.mha_bwd_workspace_size.restype = ctypes.c_size_t
+        L.mha_fwd_tile_order.argtypes = [i, i, i, i, i, i, ctypes.POINTER(i)]
+        L.mha_fwd_tile_order.restype = i
         _lib = L
     return _lib
 
@@ -187,6 +189,18 @@ def mha_fwd_paged(q, k_cache, v_cache, block_table, seq_lens, o, lse, B: int, H:
 
 def mha_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(lib().mha_bwd_workspace_size(int(B), int(H), int(N), int(d)))
+
+
+def mha_fwd_tile_order(B: int, H: int, N: int, d: int, causal: bool, sms: int) -> int:
+    """C ``mha_fwd_tile_order``: 0 for the default work order, 1 for the
+    head-major one, as mha_fwd would launch on a device with ``sms``
+    multiprocessors (host only, no CUDA call)."""
+    order = ctypes.c_int(-1)
+    rc = lib().mha_fwd_tile_order(int(B), int(H), int(N), int(d), int(bool(causal)), int(sms),
+                                  ctypes.byref(order))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_fwd_tile_order")
+    return int(order.value)
 
 
 def mha_bwd(q, k, v, o, lse, dout, dq, dk, dv, B: int, H: int, N: int, d: int, scale: float,

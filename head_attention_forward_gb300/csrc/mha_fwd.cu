@@ -396,6 +396,15 @@ int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   return err == cudaSuccess ? MHA_OK : MHA_ERR_CUDA;
 }
 
+int mha_fwd_tile_order(int B, int H, int N, int d, int causal, int sms, int* order) {
+  if (B < 0 || H < 0 || N < 0 || sms <= 0 || order == nullptr) return MHA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return MHA_ERR_UNSUPPORTED_DIM;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
+  *order = (BH > 0 && N > 0 && use_head_major(static_cast<int>(BH), N, d, causal != 0, sms)) ? 1 : 0;
+  return MHA_OK;
+}
+
 int mha_device_status(void* stream, int reset, unsigned* detail) {
   int dev = 0;
   unsigned* status = nullptr;

@@ -231,6 +231,22 @@ const char *mha_strerror(int status);
 int mha_device_status(void *stream, int reset, unsigned *detail);
 
 /*
+ * mha_fwd_tile_order - which work order mha_fwd uses for a shape; host
+ * only, no CUDA call.  *order = 0: the default order (work tiles of 256
+ * query rows, heads fastest, causal m-blocks heaviest first, dealt to the
+ * persistent CTAs in snake rounds); *order = 1: the head-major order (the
+ * m-blocks of one head adjacent; under the causal mask a CTA takes m-blocks
+ * M-1-i and i of a head together), which keeps the K/V of the few heads in
+ * flight in L2.  mha_fwd picks 1 when d == 128, all heads' K/V
+ * (2*B*H*N*d*2 bytes) exceed 96 MiB, and its rounds of equal work items
+ * fill at least 95% of the grid's slots.  `sms` is the multiprocessor count
+ * that mha_fwd takes from the current device (152 on a GB300).
+ * Errors: MHA_ERR_INVALID_ARG for a negative size, sms <= 0 or a null
+ * `order`; MHA_ERR_UNSUPPORTED_DIM unless d is 64 or 128.
+ */
+int mha_fwd_tile_order(int B, int H, int N, int d, int causal, int sms, int *order);
+
+/*
  * mha_set_wait_limit - set the cycle budget of every device-side wait for
  * launches made after this call (default 2^31 SM cycles, about one second).
  * `cycles` must be > 0.  Affects only this process.

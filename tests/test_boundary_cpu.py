@@ -215,3 +215,30 @@ def test_bwd_argument_checks(L):
     assert call(dv=7 * big) == mha.MHA_ERR_INVALID_ARG         # dv over dq
     assert call(ws=9 * big) == mha.MHA_ERR_INVALID_ARG         # workspace over dv
     assert call(N=0) == mha.MHA_OK and call(B=0) == mha.MHA_OK
+
+
+@pytest.mark.parametrize("shape,order", [
+    ((1, 2, 128, 64, False), 0), ((16, 16, 512, 64, False), 0), ((4, 16, 2048, 64, True), 0),
+    ((2, 32, 4096, 128, False), 1),   # 128 MiB of K/V, 1024 equal tiles fill 96% of 7 rounds
+    ((2, 32, 4096, 128, True), 0),    # 512 equal pairs would fill only 84% of 4 rounds
+    ((1, 32, 16384, 128, True), 1),   # 256 MiB, 1024 pairs: 96%
+    ((1, 32, 16603, 128, True), 1),   # odd m-block count: 1056 items, 7 rounds, 99%
+    ((2, 32, 4000, 128, False), 1),
+    ((1, 32, 16384, 64, True), 0),    # d = 64 always takes the default order
+    ((1, 8, 4096, 128, True), 0),     # 32 MiB of K/V fits in L2
+])
+def test_fwd_tile_order(L, shape, order):
+    """The work order mha_fwd chooses, from the host-only query."""
+    import head_attention_forward_gb300 as mha
+    B, H, N, d, causal = shape
+    assert mha.mha_fwd_tile_order(B, H, N, d, causal, 152) == order
+
+
+def test_fwd_tile_order_argument_checks(L):
+    import head_attention_forward_gb300 as mha
+    out = ctypes.c_int(7)
+    assert L.mha_fwd_tile_order(1, 1, 8, 96, 0, 152, ctypes.byref(out)) == mha.MHA_ERR_UNSUPPORTED_DIM
+    assert L.mha_fwd_tile_order(-1, 1, 8, 64, 0, 152, ctypes.byref(out)) == mha.MHA_ERR_INVALID_ARG
+    assert L.mha_fwd_tile_order(1, 1, 8, 64, 0, 0, ctypes.byref(out)) == mha.MHA_ERR_INVALID_ARG
+    assert L.mha_fwd_tile_order(1, 1, 8, 64, 0, 152, None) == mha.MHA_ERR_INVALID_ARG
+    assert L.mha_fwd_tile_order(0, 1, 8, 128, 1, 152, ctypes.byref(out)) == mha.MHA_OK and out.value == 0

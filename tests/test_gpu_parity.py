@@ -150,3 +150,24 @@ def test_head_major_order(shape):
     slack = 1e-2 + 1e-2 * vt.abs().amax()
     assert bool(((ot <= hi + slack) & (ot >= lo - slack)).all())
     assert np.isfinite(lse).all()
+
+
+@pytest.mark.parametrize("shape", [(1, 32, 16384, True), (2, 32, 4096, False)], ids=["N16384-causal", "N4096"])
+def test_head_major_matches_snake_bit_for_bit(shape):
+    """A row's arithmetic does not depend on which CTA computes it or when,
+    so the head-major order must give the same bits as the snake order.  The
+    full shape runs head-major (its K/V exceed L2); slices of four heads, run
+    on their own, have K/V that fit in L2 and run in the snake order."""
+    import head_attention_forward_gb300 as mha
+    B, H, N, causal = shape
+    d = 128
+    assert mha.mha_fwd_tile_order(B, H, N, d, causal, 152) == 1
+    q, k, v = synth.qkv(50 + N, B, H, N, d)
+    o, lse = run_gpu(q, k, v, causal)
+    for b in range(B):
+        for h0 in (0, H - 4):
+            assert mha.mha_fwd_tile_order(1, 4, N, d, causal, 152) == 0
+            sl = (slice(b, b + 1), slice(h0, h0 + 4))
+            o_s, lse_s = run_gpu(q[sl], k[sl], v[sl], causal)
+            assert np.array_equal(o_s, o[sl]), (b, h0)
+            assert np.array_equal(lse_s, lse[sl]), (b, h0)

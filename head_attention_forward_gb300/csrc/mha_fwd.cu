@@ -343,6 +343,8 @@ int mha_fwd(const void* q, const void* k, const void* v, void* o, float* lse, in
   const long long BH = static_cast<long long>(B) * H;
   if (BH == 0 || N == 0) return MHA_OK;
   if (BH > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
+  // the kernel counts work tiles (and their positions past the end) in int
+  if (BH * ((N + 255) / 256) > (1ll << 30)) return MHA_ERR_INVALID_ARG;
   if (!q || !k || !v || !o || !lse) return MHA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return MHA_ERR_MISALIGNED;

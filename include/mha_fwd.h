@@ -58,7 +58,9 @@ typedef enum {
  *   o       : bf16 [B, H, N, d], device, written (rounded to nearest even).
  *   lse     : fp32 [B, H, N], device, written: LSE_i as defined above.
  *   B, H, N : batch, heads, sequence length (queries = keys = N), each >= 0.
- *             B*H*N == 0 is a no-op that returns MHA_OK.
+ *             B*H*N == 0 is a no-op that returns MHA_OK.  B*H <= INT_MAX and
+ *             B*H*ceil(N/256) <= 2^30 (tensors of that size would not fit
+ *             in device memory), else MHA_ERR_INVALID_ARG.
  *   d       : head dimension, 64 or 128.
  *   scale   : score multiplier, finite and > 0 (usually 1/sqrt(d) in fp32).
  *   causal  : 0 = every key; non-zero = key j > query i excluded (square,

@@ -67,6 +67,9 @@ def test_argument_checks(L):
     assert _fwd(L, **dict(ok, k=2 * big + 8)) == mha.MHA_ERR_MISALIGNED
     assert _fwd(L, **dict(ok, o=big)) == mha.MHA_ERR_INVALID_ARG  # o aliases q
     assert _fwd(L, **dict(ok, lse=2 * big + 64)) == mha.MHA_ERR_INVALID_ARG  # lse inside k
+    # sizes past the int counters (far beyond any device memory)
+    assert _fwd(L, **ok, B=1 << 16, H=1 << 16) == mha.MHA_ERR_INVALID_ARG  # B*H > INT_MAX
+    assert _fwd(L, **ok, B=1 << 15, H=1 << 15, N=257) == mha.MHA_ERR_INVALID_ARG  # 2^31 work tiles
     # empty problems return before any CUDA call
     assert _fwd(L, **ok, N=0) == mha.MHA_OK
     assert _fwd(L, **ok, B=0) == mha.MHA_OK

@@ -111,6 +111,29 @@ def test_sharp_softmax_rescaling(d):
         assert_close(o, lse, o_ref, lse_ref, f"sharp d={d} causal={causal}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_running_max_paths(d):
+    """Scores g_i * f_j with f rising along the keys and a slope g_i per row
+    drawn from [-30, 30]: in one warp some rows' maxima fall behind (every
+    term of a later tile below 1), some rise by less than the rescale
+    threshold per 128-key tile (terms above 1, no rescale) and some by more
+    (a rescale), so every branch of the softmax step meets every other."""
+    B, H, N = 1, 2, 1024
+    rng = np.random.default_rng(123 + d)
+    g = rng.uniform(-30.0, 30.0, size=(B, H, N)).astype(np.float32)
+    f = np.linspace(0.0, 25.0, N, dtype=np.float32)
+    qf = rng.standard_normal((B, H, N, d)).astype(np.float32) * 0.1
+    kf = rng.standard_normal((B, H, N, d)).astype(np.float32) * 0.1
+    qf[..., 0] = g
+    kf[..., 0] = f[None, None, :]
+    q, k = synth.f32_to_bf16_bits(qf), synth.f32_to_bf16_bits(kf)
+    v = synth.f32_to_bf16_bits(rng.standard_normal((B, H, N, d)).astype(np.float32))
+    for causal in (False, True):
+        o, lse = run_gpu(q, k, v, causal)
+        o_ref, lse_ref = oracle.attention_fwd(q, k, v, scale_for(d), causal)
+        assert_close(o, lse, o_ref, lse_ref, f"ramp d={d} causal={causal}")
+
+
 @pytest.mark.parametrize("shape", [(1, 32, 16603, True), (2, 32, 4000, False)],
                          ids=["causal-odd-mblocks", "noncausal-ragged"])
 def test_head_major_order(shape):

@@ -81,6 +81,26 @@ def test_splitkv_split_counts(splits):
     compare(o, lse, o_ref, lse_ref, f"splits={splits}")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_splitkv_running_max_paths(d, splits):
+    """Scores g_i * f_j with f rising along the keys and per-query slopes
+    g_i from [-30, 30]: within one warp some rows' maxima fall behind, some
+    rise by less than the rescale threshold per tile and some by more."""
+    B, H, Nq, Nk = 1, 3, 16, 3000
+    rng = np.random.default_rng(321 + d + splits)
+    qf = rng.standard_normal((B, H, Nq, d)).astype(np.float32) * 0.1
+    kf = rng.standard_normal((B, H, Nk, d)).astype(np.float32) * 0.1
+    qf[..., 0] = rng.uniform(-30.0, 30.0, size=(B, H, Nq))
+    kf[..., 0] = np.linspace(0.0, 100.0, Nk, dtype=np.float32)[None, None, :]
+    q, k = synth.f32_to_bf16_bits(qf), synth.f32_to_bf16_bits(kf)
+    v = synth.f32_to_bf16_bits(rng.standard_normal((B, H, Nk, d)).astype(np.float32))
+    for causal in (False, True):
+        o, lse = run_kv(q, k, v, causal, num_splits=splits)
+        o_ref, lse_ref = oracle.attention_kv(q, k, v, scale_for(d), causal)
+        compare(o, lse, o_ref, lse_ref, f"ramp d={d} splits={splits} causal={causal}")
+
+
 def test_splitkv_square_matches_fused():
     """With Nq == Nk <= 16 both entry points compute the same rows."""
     import torch

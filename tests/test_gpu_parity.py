@@ -81,10 +81,41 @@ def test_config_sampled(name):
     assert np.isfinite(lse).all()
 
 
+@pytest.mark.parametrize("shape", [(1, 8, 65536, 128, True), (1, 2, 65536, 64, False)],
+                         ids=["N65536-d128-causal", "N65536-d64"])
+def test_long_sequence(shape):
+    """A 65536-token sequence: 512 K/V tiles per row and 256 m-blocks per
+    head (at d = 128 all heads' K/V, 268 MB, exceed L2, so the head-major
+    order runs).  Sampled rows of three heads against the oracle, including the
+    first and last rows and rows at m-block edges; every output finite."""
+    import head_attention_forward_gb300 as mha
+    B, H, N, d, causal = shape
+    q, k, v = synth.qkv(7000 + d, B, H, N, d)
+    if d == 128:
+        assert mha.mha_fwd_tile_order(B, H, N, d, causal, 152) == 1
+    o, lse = run_gpu(q, k, v, causal)
+    assert np.isfinite(o).all() and np.isfinite(lse).all()
+    rng = np.random.default_rng(77)
+    heads = sorted({0, B * H - 1, int(rng.integers(1, B * H))})
+    o_all, l_all, o_ref_all, l_ref_all = [], [], [], []
+    for bh in heads:
+        rows = _sample_rows(N, rng)
+        o_ref, lse_ref = oracle.attention_rows(q, k, v, scale_for(d), causal, int(bh), rows)
+        o_all.append(o.reshape(B * H, N, d)[bh][rows])
+        l_all.append(lse.reshape(B * H, N)[bh][rows])
+        o_ref_all.append(o_ref)
+        l_ref_all.append(lse_ref)
+    assert_close(np.concatenate(o_all), np.concatenate(l_all), np.concatenate(o_ref_all),
+                 np.concatenate(l_ref_all), f"N={N} d={d} causal={causal}")
+
+
 SHAPES = [
     # (B, H, N, d)
     (1, 1, 1, 64), (1, 1, 2, 128), (1, 2, 127, 64), (2, 1, 129, 128), (1, 1, 255, 64),
     (1, 1, 256, 128), (1, 3, 257, 64), (1, 1, 384, 128), (2, 2, 640, 64), (1, 1, 1000, 128),
+    # many small heads: thousands of work tiles per launch, 1-2 K/V tiles each,
+    # and (N = 100) no rows for the second stage
+    (64, 64, 100, 64), (16, 64, 200, 128),
 ]
 
 

@@ -403,6 +403,7 @@ int mha_fwd_tile_order(int B, int H, int N, int d, int causal, int sms, int* ord
   if (d != 64 && d != 128) return MHA_ERR_UNSUPPORTED_DIM;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffll) return MHA_ERR_INVALID_ARG;
+  if (BH * ((N + 255) / 256) > (1ll << 30)) return MHA_ERR_INVALID_ARG;  // as mha_fwd
   *order = (BH > 0 && N > 0 && use_head_major(static_cast<int>(BH), N, d, causal != 0, sms)) ? 1 : 0;
   return MHA_OK;
 }

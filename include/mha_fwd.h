@@ -243,8 +243,9 @@ int mha_device_status(void *stream, int reset, unsigned *detail);
  * (2*B*H*N*d*2 bytes) exceed 96 MiB, and its rounds of equal work items
  * fill at least 95% of the grid's slots.  `sms` is the multiprocessor count
  * that mha_fwd takes from the current device (152 on a GB300).
- * Errors: MHA_ERR_INVALID_ARG for a negative size, sms <= 0 or a null
- * `order`; MHA_ERR_UNSUPPORTED_DIM unless d is 64 or 128.
+ * Errors: MHA_ERR_INVALID_ARG for a negative size, sms <= 0, a null
+ * `order` or the sizes mha_fwd rejects; MHA_ERR_UNSUPPORTED_DIM unless d
+ * is 64 or 128.
  */
 int mha_fwd_tile_order(int B, int H, int N, int d, int causal, int sms, int *order);
 

@@ -245,3 +245,5 @@ def test_fwd_tile_order_argument_checks(L):
     assert L.mha_fwd_tile_order(1, 1, 8, 64, 0, 0, ctypes.byref(out)) == mha.MHA_ERR_INVALID_ARG
     assert L.mha_fwd_tile_order(1, 1, 8, 64, 0, 152, None) == mha.MHA_ERR_INVALID_ARG
     assert L.mha_fwd_tile_order(0, 1, 8, 128, 1, 152, ctypes.byref(out)) == mha.MHA_OK and out.value == 0
+    # the sizes mha_fwd rejects (2^31 work tiles)
+    assert L.mha_fwd_tile_order(1 << 15, 1 << 15, 257, 128, 1, 152, ctypes.byref(out)) == mha.MHA_ERR_INVALID_ARG
